@@ -1,0 +1,256 @@
+/*
+ * moe_oracle.c -- plain, slow, single-threaded CPU oracle for the MoE
+ * expert-FFN decode layer and for moe_align_block_size.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, calls or
+ * includes this file; only tests/, __graft_entry__.smoke() and bench.py's
+ * cpu_baseline / reference legs load it.  It shares no code, header, table
+ * or constant with the CUDA path.
+ *
+ * Everything floating-point is FP64.  Each function names the passage of the
+ * source pages it follows:
+ *   [WD]  "Warp decode" (cursor.com blog, zh-Hant), sections
+ *         "兩個 kernel 的運作方式" (how the two kernels work) and
+ *         "準確度改進" (accuracy: BF16 activations, FP32 accumulation).
+ *   [AS]  "AMD GPU性能暴涨7倍 ... 高效MoE支持任意专家数量" (aizws.net), sections
+ *         on MoE Align & Sort and "编写对AMD设备友好的CUDA实现" (the D-C-P
+ *         counting / cumsum / placement algorithm).
+ *   [MX]  MXFP8 as the decode page names it: E4M3 elements with one E8M0
+ *         scale per 32 consecutive elements along K (OCP MX v1.0 / OFP8).
+ *
+ * Parity status: every function here is pinned by tests/test_oracle_pins.py
+ * (exhaustive code tables, library cross-checks, a dense SwiGLU reduction,
+ * invariants, brute force).  The pages print no worked numeric example of a
+ * layer output, so the FFN is pinned by those reductions, not by page values.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_ARG (-1)
+
+/* ---------------------------------------------------------------- [MX] --- */
+
+/* OCP OFP8 E4M3 ("fn" variant: no infinities, S.1111.111 is NaN).
+ * Bias 7; exponent field 0 is subnormal: (-1)^s * 2^-6 * m/8. */
+double oracle_e4m3_decode(uint8_t q) {
+    int s = (q >> 7) & 1;
+    int e = (q >> 3) & 15;
+    int m = q & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* OCP MX E8M0 shared scale: 2^(s-127); 0xFF is NaN. */
+double oracle_e8m0_decode(uint8_t s) {
+    if (s == 0xFF) return NAN;
+    return ldexp(1.0, (int)s - 127);
+}
+
+/* dequantised weight element: e4m3(q) * 2^(scale-127) [MX] */
+static double deq(const uint8_t* w, const uint8_t* sc, int64_t K, int64_t row, int64_t col) {
+    return oracle_e4m3_decode(w[row * K + col]) * oracle_e8m0_decode(sc[row * (K / 32) + col / 32]);
+}
+
+/* ------------------------------------------------------- BF16 helpers --- */
+
+double oracle_bf16_to_double(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/* Round a double to the nearest BF16 (ties to even), in one rounding step.
+ * bf16 keeps 8 significant bits; its exponent range is that of binary32
+ * (normal down to 2^-126, subnormal step 2^-133).  The quantum for |v| in
+ * [2^e, 2^(e+1)) is 2^(e-7), floored at 2^-133; rint() is round-half-even
+ * under the default rounding mode and v/quantum is exact in binary64. */
+uint16_t oracle_bf16_round(double v) {
+    if (isnan(v)) return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (isinf(a)) return sign | 0x7F80;
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);           /* a = f * 2^e, f in [0.5, 1) -> floor(log2 a) = e-1 */
+    int lead = e - 1;
+    if (lead < -126) lead = -126;
+    double quantum = ldexp(1.0, lead - 7);
+    double r = rint(a / quantum) * quantum;
+    /* largest finite bf16 = (2 - 2^-7) * 2^127 */
+    if (r > ldexp(2.0 - ldexp(1.0, -7), 127)) return sign | 0x7F80;
+    float rf = (float)r;    /* exact: r has <= 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &rf, 4);
+    return sign | (uint16_t)((u >> 16) & 0x7FFF);
+}
+
+/* ---------------------------------------------------------------- [WD] --- */
+
+static double silu(double g) { return g / (1.0 + exp(-g)); }
+
+/* One expert's gate/up pass for one token.
+ *  [WD] gate/up kernel: the routed expert's gate row and up row are both
+ *  dotted with the same activation vector, then SiLU(gate) * up gives one
+ *  intermediate value per (token, expert, neuron); the intermediate is
+ *  BF16 (the pages keep activations in BF16 throughout).
+ *  hf_out (optional) receives the unrounded FP64 value. */
+static void gate_up_one(const uint16_t* xb, int64_t d, const uint8_t* wg, const uint8_t* sg,
+                        const uint8_t* wu, const uint8_t* su, int64_t I, int64_t e,
+                        uint16_t* h_out, double* hf_out) {
+    const uint8_t* wge = wg + e * I * d;
+    const uint8_t* sge = sg + e * I * (d / 32);
+    const uint8_t* wue = wu + e * I * d;
+    const uint8_t* sue = su + e * I * (d / 32);
+    for (int64_t n = 0; n < I; ++n) {
+        double g = 0.0, u = 0.0;
+        for (int64_t c = 0; c < d; ++c) {
+            double xv = oracle_bf16_to_double(xb[c]);
+            g += xv * deq(wge, sge, d, n, c);
+            u += xv * deq(wue, sue, d, n, c);
+        }
+        double hf = silu(g) * u;
+        if (hf_out) hf_out[n] = hf;
+        if (h_out) h_out[n] = oracle_bf16_round(hf);
+    }
+}
+
+/* One expert's down projection of one intermediate vector, FP64. */
+static void down_one(const double* hv, int64_t I, const uint8_t* wd, const uint8_t* sd, int64_t d,
+                     int64_t e, double scale, double* y) {
+    const uint8_t* wde = wd + e * d * I;
+    const uint8_t* sde = sd + e * d * (I / 32);
+    for (int64_t o = 0; o < d; ++o) {
+        double acc = 0.0;
+        for (int64_t i = 0; i < I; ++i) acc += hv[i] * deq(wde, sde, I, o, i);
+        y[o] += scale * acc;
+    }
+}
+
+/*
+ * The whole decode layer [WD]:
+ *   for each token b and routed slot j (e = topk_ids[b,j]):
+ *       h[b,j,:] = bf16( SiLU(Wg[e] x_b) * (Wu[e] x_b) )
+ *   y64[b,:] = sum_j topk_w[b,j] * Wd[e_j] h[b,j,:]
+ *              + (shared expert present) 1.0 * Wsd h[b,k,:]
+ * with h[b,k,:] the shared expert's intermediate.  y64 is left unrounded.
+ * truth64 (optional) is the same computation with h kept in FP64.
+ * h_bf16 (optional) receives the BF16 intermediates, layout [B][k+S][I].
+ * Shared-expert arrays are NULL when there is no shared expert; the shared
+ * expert has the same I and d as the routed ones.
+ * Returns ORACLE_ERR_ARG on a bad shape or an expert id outside [0, E).
+ */
+int oracle_moe_layer(const uint16_t* x, int B, int d, const int32_t* topk_ids, const float* topk_w,
+                     int k, const uint8_t* wg, const uint8_t* sg, const uint8_t* wu,
+                     const uint8_t* su, const uint8_t* wd, const uint8_t* sd, int E, int I,
+                     const uint8_t* shg, const uint8_t* shsg, const uint8_t* shu,
+                     const uint8_t* shsu, const uint8_t* shd, const uint8_t* shsd,
+                     uint16_t* h_bf16, double* y64, double* truth64) {
+    if (B < 0 || d <= 0 || I <= 0 || k < 0 || E <= 0 || d % 32 || I % 32) return ORACLE_ERR_ARG;
+    int S = (shg != NULL) ? 1 : 0;
+    int slots = k + S;
+    uint16_t* hb = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
+    double* hf = (double*)malloc(sizeof(double) * (size_t)I);
+    double* hr = (double*)malloc(sizeof(double) * (size_t)I);
+    if (!hb || !hf || !hr) {
+        free(hb); free(hf); free(hr);
+        return ORACLE_ERR_ARG;
+    }
+    int rc = ORACLE_OK;
+    for (int b = 0; b < B && rc == ORACLE_OK; ++b) {
+        const uint16_t* xb = x + (int64_t)b * d;
+        double* yb = y64 + (int64_t)b * d;
+        double* tb = truth64 ? truth64 + (int64_t)b * d : NULL;
+        for (int o = 0; o < d; ++o) {
+            yb[o] = 0.0;
+            if (tb) tb[o] = 0.0;
+        }
+        for (int j = 0; j < slots; ++j) {
+            int shared = (j == k);
+            int64_t e = shared ? 0 : topk_ids[(int64_t)b * k + j];
+            if (!shared && (e < 0 || e >= E)) { rc = ORACLE_ERR_ARG; break; }
+            double wt = shared ? 1.0 : (double)topk_w[(int64_t)b * k + j];
+            gate_up_one(xb, d, shared ? shg : wg, shared ? shsg : sg, shared ? shu : wu,
+                        shared ? shsu : su, I, e, hb, hf);
+            for (int i = 0; i < I; ++i) hr[i] = oracle_bf16_to_double(hb[i]);
+            if (h_bf16) memcpy(h_bf16 + ((int64_t)b * slots + j) * I, hb, sizeof(uint16_t) * (size_t)I);
+            down_one(hr, I, shared ? shd : wd, shared ? shsd : sd, d, e, wt, yb);
+            if (tb) down_one(hf, I, shared ? shd : wd, shared ? shsd : sd, d, e, wt, tb);
+        }
+    }
+    free(hb); free(hf); free(hr);
+    return rc;
+}
+
+/* ---------------------------------------------------------------- [AS] --- */
+
+/* Sizes of the align outputs: the padded buffer is the worst case in which
+ * every expert's segment needs block_size-1 pad entries. */
+int oracle_align_sizes(int T, int k, int E, int block_size, int64_t* n_sorted, int64_t* n_blocks) {
+    if (T < 0 || k < 0 || E <= 0 || block_size <= 0) return ORACLE_ERR_ARG;
+    int64_t n = (int64_t)T * k + (int64_t)E * (block_size - 1);
+    *n_sorted = n;
+    *n_blocks = (n + block_size - 1) / block_size;
+    return ORACLE_OK;
+}
+
+/*
+ * moe_align_block_size [AS]: sort the flat (token, slot) indices f = t*k + j
+ * by expert id, pad each expert's run up to a multiple of block_size with the
+ * sentinel T*k, and record which expert owns each block_size-sized block.
+ * Step by step, in the page's D-C-P order, done serially:
+ *   count   cnt[e] = #{f : ids[f] == e}
+ *   cumsum  pad[e] = ceil(cnt[e]/bs)*bs ; start = exclusive prefix of pad
+ *   place   walk f in increasing order: sorted[start[e] + pos[e]++] = f
+ * Ties are therefore broken by flat index (a stable counting sort).
+ * Entries past num_tokens_post_pad hold the sentinel; expert_ids past
+ * num_tokens_post_pad/bs hold -1.
+ */
+int oracle_align(const int32_t* ids, int T, int k, int E, int block_size, int32_t* sorted,
+                 int64_t n_sorted, int32_t* expert_ids, int64_t n_blocks, int32_t* ntpp) {
+    int64_t need_sorted, need_blocks;
+    if (oracle_align_sizes(T, k, E, block_size, &need_sorted, &need_blocks) != ORACLE_OK)
+        return ORACLE_ERR_ARG;
+    if (n_sorted < need_sorted || n_blocks < need_blocks) return ORACLE_ERR_ARG;
+    int64_t N = (int64_t)T * k;
+    int64_t* cnt = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+    int64_t* start = (int64_t*)calloc((size_t)E + 1, sizeof(int64_t));
+    int64_t* pos = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+    if (!cnt || !start || !pos) {
+        free(cnt); free(start); free(pos);
+        return ORACLE_ERR_ARG;
+    }
+    int rc = ORACLE_OK;
+    for (int64_t f = 0; f < N; ++f) {
+        int32_t e = ids[f];
+        if (e < 0 || e >= E) { rc = ORACLE_ERR_ARG; break; }
+        cnt[e] += 1;
+    }
+    if (rc == ORACLE_OK) {
+        for (int e = 0; e < E; ++e) {
+            int64_t padded = (cnt[e] + block_size - 1) / block_size * block_size;
+            start[e + 1] = start[e] + padded;
+        }
+        for (int64_t i = 0; i < n_sorted; ++i) sorted[i] = (int32_t)N;
+        for (int64_t f = 0; f < N; ++f) {
+            int32_t e = ids[f];
+            sorted[start[e] + pos[e]] = (int32_t)f;
+            pos[e] += 1;
+        }
+        for (int64_t blk = 0; blk < n_blocks; ++blk) expert_ids[blk] = -1;
+        for (int e = 0; e < E; ++e)
+            for (int64_t p = start[e]; p < start[e + 1]; p += block_size)
+                expert_ids[p / block_size] = e;
+        *ntpp = (int32_t)start[E];
+    }
+    free(cnt); free(start); free(pos);
+    return rc;
+}
