@@ -1,0 +1,209 @@
+/*
+ * moedec.h -- C ABI of libmoedec.so, a GB300 (sm_103a) small-batch
+ * mixture-of-experts expert-FFN decode layer with MXFP8 weights, plus the
+ * expert-centric align-and-sort bookkeeping.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [WD] "Warp decode" (cursor.com blog): the decode layer as two passes --
+ *        a fused gate/up pass (section "兩個 kernel 的運作方式", how the two
+ *        kernels work) and a down pass that folds every routed expert's
+ *        routing weight into one FP32 accumulator per output value, with no
+ *        gather buffer, per-expert output buffer or separate combine
+ *        (sections "消除緩衝區" eliminating buffers, "準確度改進" accuracy).
+ *   [AS] "AMD GPU性能暴涨7倍 ... 高效MoE支持任意专家数量" (aizws.net): MoE
+ *        Align & Sort and its multi-block count / cumsum / placement
+ *        algorithm (section "编写对AMD设备友好的CUDA实现").
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers unless the name says _host.
+ *     The caller owns every buffer; the library never allocates device or
+ *     host memory and never frees anything.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  Host-side argument checks happen before any launch;
+ *     a call that returns an error has launched nothing.
+ *   - Return value: MOE_OK (0) or a negative MOE_ERR_* code; moe_strerror()
+ *     names it.
+ *   - BF16 tensors are passed as `void*` (raw 16-bit patterns).
+ *   - MXFP8 weights: one byte per element holding an E4M3 code (OCP OFP8,
+ *     no infinities), row-major with K innermost, plus one E8M0 scale byte
+ *     per 32 consecutive elements along K (value 2^(s-127)); the scale
+ *     array is row-major [rows][K/32].  K must be a multiple of 32.
+ *   - Device-side input checks: an expert id outside [0, E) never causes
+ *     an out-of-bounds access; the slot is skipped and a sticky device error
+ *     bit is set, which moe_device_error() reports.
+ */
+#ifndef MOEDEC_H
+#define MOEDEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* identical to cudaStream_t */
+
+enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_ARG = -1,       /* NULL pointer where one is required, negative size */
+    MOE_ERR_SHAPE = -2,     /* d or I not a multiple of 32, k > E, ... */
+    MOE_ERR_LIMIT = -3,     /* beyond a documented limit of the decode kernels */
+    MOE_ERR_WORKSPACE = -4, /* workspace missing or smaller than required */
+    MOE_ERR_ALIGN = -5,     /* pointer not aligned as documented */
+    MOE_ERR_CUDA = -6,      /* a CUDA runtime call or launch failed */
+    MOE_ERR_DEVICE = -7     /* a kernel flagged bad input (see moe_device_error) */
+};
+
+/* Device error bits reported by moe_device_error(). */
+#define MOE_DEVERR_EXPERT_ID 0x1 /* an expert id outside [0, E) was skipped */
+
+/* Limits of the decode kernels (moe_gate_up, moe_down, moe_layer*). */
+#define MOE_MAX_EXPERTS 1024  /* E */
+#define MOE_MAX_TOKENS 256    /* B */
+#define MOE_MAX_SLOTS 2048    /* B * k */
+/* Limits of moe_align_block_size. */
+#define MOE_ALIGN_MAX_EXPERTS 1024
+
+/* One MXFP8 weight tensor: codes [E][rows][K] and scales [E][rows][K/32].
+ * Both device pointers; `w` must be 32-byte aligned (K % 32 == 0 then keeps
+ * every row 32-byte aligned). */
+typedef struct {
+    const uint8_t* w;
+    const uint8_t* s;
+} moe_mx_t;
+
+/* Library version: major*10000 + minor*100 + patch. */
+int moe_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* moe_strerror(int status);
+
+/*
+ * moe_gate_up -- fused gate/up pass [WD, how the two kernels work].
+ *   For each token b < B, routed slot j < k (expert e = topk_ids[b*k+j])
+ *   and, when a shared expert is given, slot j = k (the shared expert),
+ *   and each intermediate neuron n < I:
+ *     g = sum_c x[b,c] * deq(Wg[e,n,c]),  u = sum_c x[b,c] * deq(Wu[e,n,c])
+ *     h[b,j,n] = bf16_rn( g * sigmoid(g) * u )
+ *   with deq() the MXFP8 dequantisation, FP32 products and accumulation.
+ *   x reads once per distinct expert; each weight row is streamed once.
+ * Arguments
+ *   x         BF16 [B][d], 16-byte aligned.
+ *   topk_ids  int32 [B][k].
+ *   w_gate    MXFP8 [E][I][d];  w_up  MXFP8 [E][I][d].
+ *   shared_gate, shared_up: NULL for no shared expert, else MXFP8 [1][I][d]
+ *             (both or neither).
+ *   h         BF16 [B][k+S][I] output (S = 1 with a shared expert), 4-byte
+ *             aligned.  Every element is written.
+ * Limits: B <= MOE_MAX_TOKENS, B*k <= MOE_MAX_SLOTS, E <= MOE_MAX_EXPERTS,
+ *   1 <= k <= E, d and I multiples of 32.  B == 0 is a no-op.
+ */
+int moe_gate_up(const void* x, int B, int d, const int32_t* topk_ids, int k, moe_mx_t w_gate,
+                moe_mx_t w_up, int E, int I, const moe_mx_t* shared_gate,
+                const moe_mx_t* shared_up, void* h, moe_stream_t stream);
+
+/*
+ * moe_down -- down pass with the routing-weighted combine folded in
+ * [WD, how the two kernels work; eliminating buffers]:
+ *   y[b,o] = bf16_rn( sum_{j<k} topk_w[b,j] * sum_i h[b,j,i] * deq(Wd[e_j,o,i])
+ *                     + S * 1.0 * sum_i h[b,k,i] * deq(Wsd[o,i]) )
+ *   one FP32 accumulator per output value across all routed experts; no
+ *   per-expert output buffer and no separate combine step.
+ * Arguments
+ *   h         BF16 [B][k+S][I] (as written by moe_gate_up), 16-byte aligned.
+ *   topk_ids  int32 [B][k];  topk_w  float32 [B][k].
+ *   w_down    MXFP8 [E][d][I];  shared_down NULL or MXFP8 [1][d][I].
+ *   y         BF16 [B][d] output; every element is written.
+ * Limits as for moe_gate_up.
+ */
+int moe_down(const void* h, int B, int k, const int32_t* topk_ids, const float* topk_w,
+             moe_mx_t w_down, int E, int d, int I, const moe_mx_t* shared_down, void* y,
+             moe_stream_t stream);
+
+/* Bytes of workspace moe_layer needs (the BF16 intermediate h). */
+int moe_layer_workspace_bytes(int B, int k, int I, int has_shared, size_t* bytes);
+
+/*
+ * moe_layer -- the whole decode layer: moe_gate_up then moe_down on the same
+ * stream, h placed at the start of `workspace` (>= moe_layer_workspace_bytes,
+ * 256-byte aligned).  Shared expert: all three shared pointers or none.
+ */
+int moe_layer(const void* x, int B, int d, const int32_t* topk_ids, const float* topk_w, int k,
+              moe_mx_t w_gate, moe_mx_t w_up, moe_mx_t w_down, int E, int I,
+              const moe_mx_t* shared_gate, const moe_mx_t* shared_up,
+              const moe_mx_t* shared_down, void* workspace, size_t workspace_bytes, void* y,
+              moe_stream_t stream);
+
+/* Bytes of device workspace moe_layer_host needs. */
+int moe_layer_host_workspace_bytes(int B, int d, int k, int I, int has_shared, size_t* bytes);
+
+/*
+ * moe_layer_host -- moe_layer with the per-step activations in HOST memory:
+ * copies x_host (BF16 [B][d]), topk_ids_host (int32 [B][k]) and topk_w_host
+ * (float32 [B][k]) to device staging inside `workspace`, runs the layer, and
+ * copies y back to y_host (BF16 [B][d]), all asynchronously on `stream`.
+ * Host buffers should be pinned (page-locked) for the copies to be
+ * asynchronous; the caller synchronises the stream before reading y_host.
+ * Weights stay device pointers.  workspace >= moe_layer_host_workspace_bytes,
+ * 256-byte aligned.
+ */
+int moe_layer_host(const void* x_host, int B, int d, const int32_t* topk_ids_host,
+                   const float* topk_w_host, int k, moe_mx_t w_gate, moe_mx_t w_up,
+                   moe_mx_t w_down, int E, int I, const moe_mx_t* shared_gate,
+                   const moe_mx_t* shared_up, const moe_mx_t* shared_down, void* workspace,
+                   size_t workspace_bytes, void* y_host, moe_stream_t stream);
+
+/*
+ * moe_align_sizes -- output and workspace sizes for moe_align_block_size:
+ *   n_sorted = T*k + E*(block_size-1)  (every expert's run padded at worst)
+ *   n_blocks = ceil(n_sorted / block_size)
+ *   ws_bytes = device workspace moe_align_block_size needs.
+ * Any of the output pointers may be NULL.
+ */
+int moe_align_sizes(int T, int k, int E, int block_size, int64_t* n_sorted, int64_t* n_blocks,
+                    size_t* ws_bytes);
+
+/*
+ * moe_align_block_size -- expert-centric bookkeeping [AS]: a stable
+ * counting sort of the flat slot indices f = t*k + j by expert id
+ * topk_ids[f], each expert's run padded to a multiple of block_size.
+ * Multi-block: per-block shared-memory histograms (count), a prefix over
+ * blocks and experts with padding (cumsum), then parallel placement.
+ * Outputs (device, int32):
+ *   sorted_token_ids [n_sorted]: expert e's flat indices in increasing f
+ *     order starting at start[e] = sum_{e'<e} pad(e'), followed by sentinel
+ *     T*k up to the padded length; entries past num_tokens_post_pad hold
+ *     T*k too.
+ *   expert_ids [n_blocks]: owning expert of each block_size block; -1 for
+ *     blocks past num_tokens_post_pad / block_size.
+ *   num_tokens_post_pad [1]: sum over experts of the padded run lengths.
+ * Every output element is written.  Ties are broken by flat index, so the
+ * result is unique and bit-exact.  workspace >= ws_bytes of
+ * moe_align_sizes, 16-byte aligned.  T*k must fit in int32.
+ * Limits: 1 <= E <= MOE_ALIGN_MAX_EXPERTS, block_size >= 1, k >= 1.
+ */
+int moe_align_block_size(const int32_t* topk_ids, int T, int k, int E, int block_size,
+                         int32_t* sorted_token_ids, int32_t* expert_ids,
+                         int32_t* num_tokens_post_pad, void* workspace, size_t workspace_bytes,
+                         moe_stream_t stream);
+
+/*
+ * moe_copy -- device-to-device copy kernel used as the HBM bandwidth
+ * reference (contiguous 32-byte loads and stores).  dst and src 32-byte
+ * aligned; bytes a multiple of 32.
+ */
+int moe_copy(void* dst, const void* src, size_t bytes, moe_stream_t stream);
+
+/*
+ * moe_device_error -- synchronise `stream`, then read and clear the sticky
+ * device error bits (MOE_DEVERR_*) of the current device into *bits.
+ * Returns MOE_ERR_DEVICE when any bit was set, MOE_OK otherwise.
+ */
+int moe_device_error(moe_stream_t stream, int* bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOEDEC_H */

@@ -1,0 +1,44 @@
+// internal.h -- launch interfaces between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moedec {
+
+struct MXView {
+    const uint8_t* w;
+    const uint8_t* s;
+};
+
+struct DecodeShape {
+    int B, k, E, d, I, S;  // S = 1 with a shared expert
+};
+
+// Device properties cached per device (SM count, shared memory per block).
+struct DeviceInfo {
+    int sm_count;
+    int max_smem_optin;
+    int* err_word;  // sticky device error bits (MOE_DEVERR_*)
+};
+cudaError_t device_info(DeviceInfo* out);
+
+cudaError_t launch_gate_up(const DecodeShape& s, const void* x, const int32_t* ids, MXView wg,
+                           MXView wu, MXView shg, MXView shu, void* h, cudaStream_t st);
+cudaError_t launch_down(const DecodeShape& s, const void* h, const int32_t* ids, const float* w,
+                        MXView wd, MXView shd, void* y, cudaStream_t st, bool after_gate_up);
+// Shared-memory bytes the decode kernels need; 0 if the shape is beyond the
+// supported limits.
+size_t gate_up_smem_bytes(const DecodeShape& s);
+size_t down_smem_bytes(const DecodeShape& s);
+
+cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int block_size, int32_t* sorted,
+                         int64_t n_sorted, int32_t* expert_ids, int64_t n_blocks, int32_t* ntpp,
+                         void* ws, cudaStream_t st);
+size_t align_workspace_bytes(int64_t n, int E);
+size_t align_smem_bytes(int E);
+
+cudaError_t launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t st);
+
+}  // namespace moedec

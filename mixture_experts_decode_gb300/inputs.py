@@ -157,6 +157,22 @@ def layer_weights(cfg: LayerConfig, device="cpu", replica: int = 0):
     return out
 
 
+def expert_weights(cfg: LayerConfig, experts, device="cpu", replica: int = 0):
+    """The weights of the listed experts only, stacked in that order: the same
+    bytes layer_weights(cfg, device, replica) holds for those experts."""
+    key = (cfg.name, "replica", replica)
+    out = {}
+    for name, rows, K in (("gate", cfg.I, cfg.d), ("up", cfg.I, cfg.d), ("down", cfg.d, cfg.I)):
+        codes, scales = [], []
+        for e in experts:
+            c, s = quantize_mx(randn((rows, K), device, *key, "w_" + name, e, std=0.02))
+            codes.append(c)
+            scales.append(s)
+        out["w_" + name] = torch.stack(codes)
+        out["s_" + name] = torch.stack(scales)
+    return out
+
+
 def layer_batch(cfg: LayerConfig, B: int, routing: str | None = None, step: int = 0):
     """(x bf16 [B, d], topk_ids int32 [B, k], topk_w float32 [B, k]) on the CPU."""
     routing = routing or cfg.routing

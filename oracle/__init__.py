@@ -34,7 +34,7 @@ def _load():
         lib.oracle_moe_layer.restype = ctypes.c_int
         lib.oracle_moe_layer.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int,
                                          P, P, P, P, P, P, ctypes.c_int, ctypes.c_int,
-                                         P, P, P, P, P, P, P, P, P]
+                                         P, P, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_align_sizes.restype = ctypes.c_int
         lib.oracle_align_sizes.argtypes = [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_int64)] * 2
         lib.oracle_align.restype = ctypes.c_int
@@ -77,7 +77,9 @@ def moe_layer(x_bf16, topk_ids, topk_w, w_gate, s_gate, w_up, s_up, w_down, s_do
     topk_w float32 [B, k]; w_* uint8 [E, rows, K] E4M3 codes; s_* uint8
     [E, rows, K/32] E8M0 scales; shared: None or a 6-tuple
     (w_gate, s_gate, w_up, s_up, w_down, s_down) with a leading dim of 1.
-    Returns dict(h=uint16 [B, k+S, I], y64=float64 [B, d], truth64=... ).
+    Returns dict(h=uint16 [B, k+S, I] (BF16 bits), h64=float64 [B, k+S, I]
+    (unrounded intermediates), g64/u64 (the gate and up dots), y64=float64
+    [B, d], truth64=... ).
     """
     lib = _load()
     x = _c(x_bf16, np.uint16)
@@ -96,14 +98,17 @@ def moe_layer(x_bf16, topk_ids, topk_w, w_gate, s_gate, w_up, s_up, w_down, s_do
         sh = [_c(a, np.uint8) for a in shared]
         S = 1
     h = np.zeros((B, k + S, I), dtype=np.uint16)
+    h64 = np.zeros((B, k + S, I), dtype=np.float64)
+    g64 = np.zeros((B, k + S, I), dtype=np.float64)
+    u64 = np.zeros((B, k + S, I), dtype=np.float64)
     y = np.zeros((B, d), dtype=np.float64)
     t = np.zeros((B, d), dtype=np.float64) if want_truth else None
     rc = lib.oracle_moe_layer(_ptr(x), B, d, _ptr(ids), _ptr(w), k, _ptr(wg), _ptr(sg), _ptr(wu),
                               _ptr(su), _ptr(wd), _ptr(sd), E, I, *(_ptr(a) for a in sh),
-                              _ptr(h), _ptr(y), _ptr(t))
+                              _ptr(h), _ptr(h64), _ptr(g64), _ptr(u64), _ptr(y), _ptr(t))
     if rc != 0:
         raise ValueError(f"oracle_moe_layer rejected its arguments (rc={rc})")
-    out = {"h": h, "y64": y}
+    out = {"h": h, "h64": h64, "g64": g64, "u64": u64, "y64": y}
     if want_truth:
         out["truth64"] = t
     return out

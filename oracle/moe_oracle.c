@@ -105,7 +105,7 @@ static double silu(double g) { return g / (1.0 + exp(-g)); }
  *  hf_out (optional) receives the unrounded FP64 value. */
 static void gate_up_one(const uint16_t* xb, int64_t d, const uint8_t* wg, const uint8_t* sg,
                         const uint8_t* wu, const uint8_t* su, int64_t I, int64_t e,
-                        uint16_t* h_out, double* hf_out) {
+                        uint16_t* h_out, double* hf_out, double* g_out, double* u_out) {
     const uint8_t* wge = wg + e * I * d;
     const uint8_t* sge = sg + e * I * (d / 32);
     const uint8_t* wue = wu + e * I * d;
@@ -118,6 +118,8 @@ static void gate_up_one(const uint16_t* xb, int64_t d, const uint8_t* wg, const 
             u += xv * deq(wue, sue, d, n, c);
         }
         double hf = silu(g) * u;
+        if (g_out) g_out[n] = g;
+        if (u_out) u_out[n] = u;
         if (hf_out) hf_out[n] = hf;
         if (h_out) h_out[n] = oracle_bf16_round(hf);
     }
@@ -143,7 +145,9 @@ static void down_one(const double* hv, int64_t I, const uint8_t* wd, const uint8
  *              + (shared expert present) 1.0 * Wsd h[b,k,:]
  * with h[b,k,:] the shared expert's intermediate.  y64 is left unrounded.
  * truth64 (optional) is the same computation with h kept in FP64.
- * h_bf16 (optional) receives the BF16 intermediates, layout [B][k+S][I].
+ * h_bf16 (optional) receives the BF16 intermediates, layout [B][k+S][I];
+ * h64 (optional) the same intermediates before rounding; g64 and u64
+ * (optional) the gate and up dot products they come from.
  * Shared-expert arrays are NULL when there is no shared expert; the shared
  * expert has the same I and d as the routed ones.
  * Returns ORACLE_ERR_ARG on a bad shape or an expert id outside [0, E).
@@ -153,7 +157,8 @@ int oracle_moe_layer(const uint16_t* x, int B, int d, const int32_t* topk_ids, c
                      const uint8_t* su, const uint8_t* wd, const uint8_t* sd, int E, int I,
                      const uint8_t* shg, const uint8_t* shsg, const uint8_t* shu,
                      const uint8_t* shsu, const uint8_t* shd, const uint8_t* shsd,
-                     uint16_t* h_bf16, double* y64, double* truth64) {
+                     uint16_t* h_bf16, double* h64, double* g64, double* u64, double* y64,
+                     double* truth64) {
     if (B < 0 || d <= 0 || I <= 0 || k < 0 || E <= 0 || d % 32 || I % 32) return ORACLE_ERR_ARG;
     int S = (shg != NULL) ? 1 : 0;
     int slots = k + S;
@@ -178,10 +183,13 @@ int oracle_moe_layer(const uint16_t* x, int B, int d, const int32_t* topk_ids, c
             int64_t e = shared ? 0 : topk_ids[(int64_t)b * k + j];
             if (!shared && (e < 0 || e >= E)) { rc = ORACLE_ERR_ARG; break; }
             double wt = shared ? 1.0 : (double)topk_w[(int64_t)b * k + j];
+            const int64_t row0 = ((int64_t)b * slots + j) * I;
             gate_up_one(xb, d, shared ? shg : wg, shared ? shsg : sg, shared ? shu : wu,
-                        shared ? shsu : su, I, e, hb, hf);
+                        shared ? shsu : su, I, e, hb, hf, g64 ? g64 + row0 : NULL,
+                        u64 ? u64 + row0 : NULL);
             for (int i = 0; i < I; ++i) hr[i] = oracle_bf16_to_double(hb[i]);
             if (h_bf16) memcpy(h_bf16 + ((int64_t)b * slots + j) * I, hb, sizeof(uint16_t) * (size_t)I);
+            if (h64) memcpy(h64 + ((int64_t)b * slots + j) * I, hf, sizeof(double) * (size_t)I);
             down_one(hr, I, shared ? shd : wd, shared ? shsd : sd, d, e, wt, yb);
             if (tb) down_one(hf, I, shared ? shd : wd, shared ? shsd : sd, d, e, wt, tb);
         }

@@ -1,0 +1,98 @@
+"""C-ABI library on the host (no GPU needed): it loads, exports every symbol
+include/moedec.h declares, and rejects bad arguments before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixture_experts_decode_gb300 as moe
+from mixture_experts_decode_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moedec.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mixture_experts_decode_gb300 import build
+    build.build()
+    return moe.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(moe_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_binding_exports():
+    assert _declared() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_strerror_and_version(lib):
+    assert lib.moe_version() >= 100
+    for code in range(0, -8, -1):
+        assert lib.moe_strerror(code).decode()
+    assert lib.moe_strerror(-99).decode() == "unknown status"
+
+
+def _mx(addr=0x10000):
+    return _lib.MXView(addr, addr)
+
+
+def _gate_up(lib, B=2, d=64, k=2, E=4, I=64, x=0x20000, ids=0x30000, h=0x40000, w=0x10000):
+    return lib.moe_gate_up(x, B, d, ids, k, _mx(w), _mx(w), E, I, None, None, h, None)
+
+
+def test_gate_up_rejects_bad_shapes_before_launch(lib):
+    assert _gate_up(lib, d=33) == -2
+    assert _gate_up(lib, I=48) == -2
+    assert _gate_up(lib, k=5, E=4) == -2
+    assert _gate_up(lib, B=-1) == -1
+    assert _gate_up(lib, B=257) == -3
+    assert _gate_up(lib, B=256, k=9, E=16) == -3
+    assert _gate_up(lib, E=1025, k=2) == -3
+    assert _gate_up(lib, x=0) == -1
+    assert _gate_up(lib, x=0x20010) == -5                # not 32-byte aligned
+    assert _gate_up(lib, w=0x10010) == -5
+    assert _gate_up(lib, B=0, x=0) == 0                  # empty batch: no-op, no launch
+
+
+def test_down_and_layer_reject_bad_arguments(lib):
+    m = _mx()
+    assert lib.moe_down(0x40000, 2, 2, 0x30000, 0x50000, m, 4, 64, 40, None, 0x60000, None) == -2
+    assert lib.moe_down(0x40000, 2, 2, 0x30000, None, m, 4, 64, 64, None, 0x60000, None) == -1
+    ws = ctypes.c_size_t()
+    assert lib.moe_layer_workspace_bytes(4, 8, 768, 1, ctypes.byref(ws)) == 0
+    assert ws.value == 4 * 9 * 768 * 2
+    assert lib.moe_layer_workspace_bytes(4, 8, 768, 0, ctypes.byref(ws)) == 0
+    small = ws.value - 1
+    rc = lib.moe_layer(0x20000, 4, 2048, 0x30000, 0x50000, 8, m, m, m, 16, 768, None, None, None,
+                       0x70000, small, 0x60000, None)
+    assert rc == -4
+    sh = ctypes.byref(m)
+    rc = lib.moe_layer(0x20000, 4, 2048, 0x30000, 0x50000, 8, m, m, m, 16, 768, sh, None, None,
+                       0x70000, 1 << 30, 0x60000, None)
+    assert rc == -1                                      # shared expert: all three or none
+
+
+def test_align_sizes_and_checks(lib):
+    ns, nb, wsb = moe.align_sizes(16384, 8, 256, 64)
+    assert (ns, nb) == (147200, 2300)                   # T*k + E*(bs-1), ceil(/bs)
+    assert wsb > 0
+    assert lib.moe_align_sizes(4, 2, 1025, 8, None, None, None) == -3
+    assert lib.moe_align_sizes(4, 2, 8, 0, None, None, None) == -1
+    assert lib.moe_align_sizes(1 << 28, 8, 8, 8, None, None, None) == -3   # exceeds int32
+    rc = lib.moe_align_block_size(0x30000, 16, 2, 8, 4, 0x40000, 0x50000, 0x60000, 0x70000, 0, None)
+    assert rc == -4
+
+
+def test_host_and_device_workspace_sizes(lib):
+    assert moe.layer_host_workspace_bytes(32, 2048, 8, 768, False) >= \
+        moe.layer_workspace_bytes(32, 8, 768, False) + 2 * 32 * 2048 * 2

@@ -205,6 +205,10 @@ def test_k1_weight1_reduces_to_dense_swiglu():
         e = ids[b, 0]
         h, y = _dense_swiglu(xf[b:b + 1], *(a[e] for a in W))
         np.testing.assert_allclose(out["truth64"][b], y[0], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(out["g64"][b, 0], xf[b] @ _dequant_np(W[0][e], W[1][e]).T,
+                                   rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(out["u64"][b, 0], xf[b] @ _dequant_np(W[2][e], W[3][e]).T,
+                                   rtol=1e-12, atol=1e-12)
         # BF16 intermediate: within half a bf16 ulp of the exact value
         hb = torch.from_numpy(out["h"][b, 0].astype(np.int16)).view(torch.bfloat16).double().numpy()
         assert np.all(np.abs(hb - h[0]) <= np.abs(h[0]) * 2.0 ** -8 + 1e-300)
