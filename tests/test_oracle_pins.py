@@ -149,18 +149,32 @@ def test_quantizer_round_trips_representable_blocks():
 
 def test_quantizer_zero_block_and_range():
     v = torch.zeros((2, 64))
-    v[1] = torch.randn(64) * 0.02
+    v[1] = torch.randn(64, generator=torch.Generator().manual_seed(11)) * 0.02
     codes, scales = inputs.quantize_mx(v)
     assert int(scales[0, 0]) == 127 and int(scales[0, 1]) == 127
     assert int(codes[0].abs().sum()) == 0
     deq = _dequant_np(codes.numpy(), scales.numpy())
-    # every block's largest element lands in [256, 448] * 2^X (E4M3 top binade)
+    # X = floor(log2 amax) - 8 puts each block's largest |v| / 2^X in [256, 512);
+    # values above 448 saturate to 448, the rest round to nearest (at most
+    # half an ulp of the top E4M3 binade, 16 * 2^X)
     for blk in range(2):
         x = v[1, blk * 32:(blk + 1) * 32].double().numpy()
         q = deq[1, blk * 32:(blk + 1) * 32]
         X = int(scales[1, blk]) - 127
-        assert 256 <= np.max(np.abs(q)) / 2.0 ** X <= 448
-        assert np.max(np.abs(q - x)) <= 2.0 ** (X + 8 - 3)    # half an E4M3 ulp at the top
+        assert 256 <= np.max(np.abs(x)) / 2.0 ** X < 512
+        sat = np.abs(x) > 448 * 2.0 ** X
+        assert np.all(np.abs(q[sat]) == 448 * 2.0 ** X)
+        assert np.all(np.abs(q[~sat] - x[~sat]) <= 16 * 2.0 ** X)
+
+
+def test_quantizer_saturates_top_binade():
+    v = torch.zeros((1, 32))
+    v[0, 0] = 500.0                    # X = 0: 500 > 448 saturates
+    v[0, 1] = -300.0
+    codes, scales = inputs.quantize_mx(v)
+    assert int(scales[0, 0]) == 127
+    assert oracle.e4m3_decode(int(codes[0, 0])) == 448.0
+    assert oracle.e4m3_decode(int(codes[0, 1])) == -288.0   # nearest E4M3 (ulp 32), ties even
 
 
 # ---------------------------------------------------------- FFN layer ---
