@@ -189,6 +189,35 @@ int moe_align_block_size(const int32_t* topk_ids, int T, int k, int E, int block
                          moe_stream_t stream);
 
 /*
+ * moe_align_block_size_static -- moe_align_block_size for callers that
+ * cannot provide device scratch memory.  (No counterpart in the source
+ * pages; this is a convenience of this library.)
+ * Some callers can only hand over their inputs and outputs: an engine that
+ * forbids device allocation after start-up, a plugin or custom-op host that
+ * owns all device memory and passes no workspace, or code that must not call
+ * cudaMalloc because it may run while a stream is being captured.  This
+ * variant needs no workspace argument: its scratch is a fixed array inside
+ * the library (MOE_ALIGN_STATIC_SCRATCH_BYTES, held on every GPU that loads
+ * the library until the process exits).  It never calls cudaMalloc,
+ * cudaFree or any other allocating routine.
+ * Arguments and outputs are those of moe_align_block_size, minus workspace.
+ * Returns MOE_ERR_LIMIT when the problem needs more scratch than the array
+ * holds (see moe_align_static_fits).  The first call on each device looks up
+ * the array's device address; make that first call before any stream
+ * capture on that device.  Every call shares the one array: each call
+ * overwrites the part it uses before reading it, but calls whose executions
+ * overlap on the GPU (different streams, or graphs replayed concurrently)
+ * race on it and must be serialised by the caller.
+ */
+#define MOE_ALIGN_STATIC_SCRATCH_BYTES (256u * 1024u)
+int moe_align_block_size_static(const int32_t* topk_ids, int T, int k, int E, int block_size,
+                                int32_t* sorted_token_ids, int32_t* expert_ids,
+                                int32_t* num_tokens_post_pad, moe_stream_t stream);
+
+/* 1 if moe_align_block_size_static can serve (T, k, E), else 0. */
+int moe_align_static_fits(int T, int k, int E);
+
+/*
  * moe_copy -- device-to-device copy kernel used as the HBM bandwidth
  * reference (contiguous 32-byte loads and stores).  dst and src 32-byte
  * aligned; bytes a multiple of 32.

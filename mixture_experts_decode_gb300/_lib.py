@@ -23,7 +23,8 @@ STATUS_NAMES = {0: "MOE_OK", -1: "MOE_ERR_ARG", -2: "MOE_ERR_SHAPE", -3: "MOE_ER
 # every symbol include/moedec.h declares
 EXPORTS = ("moe_version", "moe_strerror", "moe_gate_up", "moe_down", "moe_layer_workspace_bytes",
            "moe_layer", "moe_layer_host_workspace_bytes", "moe_layer_host", "moe_align_sizes",
-           "moe_align_block_size", "moe_copy", "moe_device_error")
+           "moe_align_block_size", "moe_align_block_size_static", "moe_align_static_fits",
+           "moe_copy", "moe_device_error")
 
 
 class MoEError(RuntimeError):
@@ -68,6 +69,8 @@ def load(path: str = LIB_PATH):
         "moe_align_sizes": ([I, I, I, I, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
                              ctypes.POINTER(S)], I),
         "moe_align_block_size": ([P, I, I, I, I, P, P, P, P, S, P], I),
+        "moe_align_block_size_static": ([P, I, I, I, I, P, P, P, P], I),
+        "moe_align_static_fits": ([I, I, I], I),
         "moe_copy": ([P, P, S, P], I),
         "moe_device_error": ([P, ctypes.POINTER(I)], I),
     }
@@ -284,6 +287,27 @@ def align_block_size(topk_ids, E: int, block_size: int, sorted_token_ids=None, e
     _check("moe_align_block_size", lib.moe_align_block_size(
         topk_ids.data_ptr(), T, k, E, block_size, sorted_token_ids.data_ptr(), expert_ids.data_ptr(),
         num_tokens_post_pad.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(dev)))
+    return sorted_token_ids, expert_ids, num_tokens_post_pad
+
+
+def align_block_size_static(topk_ids, E: int, block_size: int, sorted_token_ids=None,
+                            expert_ids=None, num_tokens_post_pad=None):
+    """moe_align_block_size_static: the same result with the library's fixed
+    scratch array instead of a caller workspace (see include/moedec.h)."""
+    lib = load()
+    dev = topk_ids.device
+    _need(topk_ids, "topk_ids", torch.int32, None, 2)
+    T, k = topk_ids.shape
+    ns, nb, _ = align_sizes(T, k, E, block_size)
+    if sorted_token_ids is None:
+        sorted_token_ids = torch.empty(ns, dtype=torch.int32, device=dev)
+    if expert_ids is None:
+        expert_ids = torch.empty(nb, dtype=torch.int32, device=dev)
+    if num_tokens_post_pad is None:
+        num_tokens_post_pad = torch.empty(1, dtype=torch.int32, device=dev)
+    _check("moe_align_block_size_static", lib.moe_align_block_size_static(
+        topk_ids.data_ptr(), T, k, E, block_size, sorted_token_ids.data_ptr(), expert_ids.data_ptr(),
+        num_tokens_post_pad.data_ptr(), _stream(dev)))
     return sorted_token_ids, expert_ids, num_tokens_post_pad
 
 

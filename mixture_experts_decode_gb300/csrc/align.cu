@@ -16,6 +16,7 @@
 // the rank comes from __match_any_sync + popc, across warps from a per-tile
 // scan over warps of per-warp expert counts.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -221,6 +222,32 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int block_size
                                                      sorted, (int)n_sorted, expert_ids,
                                                      (int)n_blocks, ntpp);
     return cudaGetLastError();
+}
+
+// ------------------------------------------- fixed-scratch variant -----
+// For callers that cannot supply device scratch: the per-block histogram
+// table lives in this file-scope array.  Host code must not pass the
+// symbol itself to a kernel (on the host it names a stand-in, not device
+// memory); it looks up the device address once per device instead.
+
+static __device__ __align__(256) int g_align_scratch[MOE_ALIGN_STATIC_SCRATCH_BYTES / sizeof(int)];
+
+cudaError_t align_static_scratch(void** out) {
+    static std::mutex mu;
+    static void* addr[64] = {nullptr};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_align_scratch);
+        if (err != cudaSuccess) return err;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return cudaSuccess;
 }
 
 }  // namespace moedec

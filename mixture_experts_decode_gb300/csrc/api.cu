@@ -294,6 +294,26 @@ int moe_align_block_size(const int32_t* topk_ids, int T, int k, int E, int block
                                     nb, num_tokens_post_pad, workspace, (cudaStream_t)stream));
 }
 
+int moe_align_static_fits(int T, int k, int E) {
+    size_t wsb = 0;
+    if (moe_align_sizes(T, k, E, 1, nullptr, nullptr, &wsb) != MOE_OK) return 0;
+    return wsb <= MOE_ALIGN_STATIC_SCRATCH_BYTES ? 1 : 0;
+}
+
+int moe_align_block_size_static(const int32_t* topk_ids, int T, int k, int E, int block_size,
+                                int32_t* sorted_token_ids, int32_t* expert_ids,
+                                int32_t* num_tokens_post_pad, moe_stream_t stream) {
+    int64_t ns = 0, nb = 0;
+    size_t wsb = 0;
+    int rc = moe_align_sizes(T, k, E, block_size, &ns, &nb, &wsb);
+    if (rc) return rc;
+    if (wsb > MOE_ALIGN_STATIC_SCRATCH_BYTES) return MOE_ERR_LIMIT;
+    void* scratch = nullptr;
+    if (align_static_scratch(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+    return moe_align_block_size(topk_ids, T, k, E, block_size, sorted_token_ids, expert_ids,
+                                num_tokens_post_pad, scratch, MOE_ALIGN_STATIC_SCRATCH_BYTES, stream);
+}
+
 int moe_copy(void* dst, const void* src, size_t bytes, moe_stream_t stream) {
     if (!dst || !src) return MOE_ERR_ARG;
     if (!aligned(dst, 32) || !aligned(src, 32) || bytes % 32) return MOE_ERR_ALIGN;

@@ -38,6 +38,8 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int block_size
                          void* ws, cudaStream_t st);
 size_t align_workspace_bytes(int64_t n, int E);
 size_t align_smem_bytes(int E);
+// Device address of the library's fixed align scratch on the current device.
+cudaError_t align_static_scratch(void** out);
 
 cudaError_t launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t st);
 
