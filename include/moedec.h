@@ -57,6 +57,7 @@ enum moe_status {
 
 /* Device error bits reported by moe_device_error(). */
 #define MOE_DEVERR_EXPERT_ID 0x1 /* an expert id outside [0, E) was skipped */
+#define MOE_DEVERR_TIMEOUT 0x2   /* a kernel's bounded wait gave up (never expected) */
 
 /* Limits of the decode kernels (moe_gate_up, moe_down, moe_layer*). */
 #define MOE_MAX_EXPERTS 1024  /* E */

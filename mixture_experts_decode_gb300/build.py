@@ -44,20 +44,23 @@ def _digest(extra) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every CUDA source and link libmoedec.so; returns its path."""
+def build(force: bool = False, verbose: bool = False, extra_flags=(), lib_path: str = LIB) -> str:
+    """Compile every CUDA source and link the library (default: the in-tree
+    libmoedec.so; extra_flags/lib_path build a variant elsewhere); returns
+    the library path."""
     extra = list(extra_flags)
     want = _digest(extra)
-    stamp = LIB + ".src-sha"
-    if not force and os.path.exists(LIB) and os.path.exists(stamp):
+    stamp = lib_path + ".src-sha"
+    if not force and os.path.exists(lib_path) and os.path.exists(stamp):
         with open(stamp) as f:
             if f.read().strip() == want:
-                return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+                return lib_path
+    obj_dir = os.path.join(BUILD_DIR, want[:12])
+    os.makedirs(obj_dir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(obj_dir, src.replace(".cu", ".o"))
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -70,15 +73,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         for _, log in results:
             if log.strip():
                 print(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib_path)
     with open(stamp, "w") as f:
         f.write(want + "\n")
-    return LIB
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -56,6 +56,20 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
     return __half22float2(hh);
 }
 
+// Four E4M3 codes (one 32-bit word, lowest byte = lowest K index) -> four
+// floats, exact.
+__device__ __forceinline__ void e4m3x4_to_float(uint32_t w, float2& lo, float2& hi) {
+    uint32_t a, b;
+    asm("{ .reg .b16 l, h;\n\t mov.b32 {l, h}, %2;\n\t cvt.rn.f16x2.e4m3x2 %0, l;\n\t cvt.rn.f16x2.e4m3x2 %1, h; }"
+        : "=r"(a), "=r"(b)
+        : "r"(w));
+    __half2 ha, hb;
+    memcpy(&ha, &a, 4);
+    memcpy(&hb, &b, 4);
+    lo = __half22float2(ha);
+    hi = __half22float2(hb);
+}
+
 // E8M0 scale byte -> 2^(s-127) as float (s = 0 gives the subnormal 2^-127;
 // s = 255, NaN in the format, is a precondition violation and yields inf).
 __device__ __forceinline__ float e8m0_to_float(uint32_t s) {
@@ -76,6 +90,136 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
     return m;
+}
+
+}  // namespace moedec
+
+namespace moedec {
+
+// ---- asynchronous global -> shared copies (per thread, 16 or 4 bytes) ----
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 16 bytes, L2 only, evict-first; src_bytes = 0 fills the destination with zeros.
+__device__ __forceinline__ void cp_async_16(void* smem, const void* gmem, int src_bytes, uint64_t pol) {
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(a), "l"(gmem),
+                 "r"(src_bytes), "l"(pol)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_4(void* smem, const void* gmem, int src_bytes) {
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(a), "l"(gmem), "r"(src_bytes) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_cached_128(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// Reduce N values across the 32 lanes of a warp in log2(N) exchange rounds
+// that each halve the values a lane holds (a butterfly reduce-scatter), then
+// finish with plain butterfly rounds.  Afterwards every lane holds the full
+// sum of value idx = (lane >> (5 - log2 N)) & (N - 1).  N is a power of two
+// <= 32.
+template <int N>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[N], int lane) {
+    int o = 16;
+#pragma unroll
+    for (int cnt = N; cnt > 1; cnt >>= 1, o >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < cnt / 2; ++i) {
+            const float send = upper ? v[i] : v[i + cnt / 2];
+            const float keep = upper ? v[i + cnt / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(FULL_MASK, send, o);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (; o >= 1; o >>= 1) r += __shfl_xor_sync(FULL_MASK, r, o);
+    return r;
+}
+
+}  // namespace moedec
+
+namespace moedec {
+
+// ---- mbarrier + bulk (TMA) copies --------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Wait for the phase with the given parity to complete.  Bounded: gives up
+// after ~2^32 SM cycles (about two seconds), returning false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    const uint32_t a = smem_addr(bar);
+    uint32_t ok = 0;
+    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(ok) : "r"(a), "r"(parity) : "memory");
+    if (ok) return true;
+    const long long t0 = clock64();
+    while (clock64() - t0 < (1ll << 32)) {
+        asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                     : "=r"(ok) : "r"(a), "r"(parity) : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
+// 1D bulk copy global -> shared, completion counted on `bar`.  dst, src
+// 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s_keep(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 }  // namespace moedec

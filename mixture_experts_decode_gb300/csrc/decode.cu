@@ -15,9 +15,12 @@
 // weight byte leaves HBM once per call even when several tokens share an
 // expert.  The token -> distinct-expert map is built in shared memory by
 // every CTA from topk_ids (no extra launch, no global buffer).
+#include <cuda.h>
+
 #include <algorithm>
-#include <mutex>
 #include <map>
+#include <mutex>
+#include <tuple>
 
 #include "common.cuh"
 #include "internal.h"
@@ -62,6 +65,7 @@ struct RouteMap {
     int* cnt;   // [E] per-expert counts, then fill cursors
     int* sid;   // [B * k] expert id of each slot (-1 if out of range)
     int* wtot;  // [DEC_WARPS] scan scratch
+    int* ucnt;  // [max_unique] slots per distinct expert after merging duplicates (down)
 };
 
 __host__ __device__ inline int max_unique(const DecodeShape& s) {
@@ -72,7 +76,7 @@ __host__ __device__ inline int n_slots(const DecodeShape& s) { return s.B * s.k 
 
 __host__ __device__ inline size_t map_ints(const DecodeShape& s, bool with_w) {
     const size_t mu = (size_t)max_unique(s);
-    size_t ints = 4 + mu + (mu + 1) + n_slots(s) + (with_w ? n_slots(s) : 0) + s.E +
+    size_t ints = 4 + mu + (mu + 1) + n_slots(s) + (with_w ? n_slots(s) + mu : 0) + s.E +
                   (size_t)s.B * s.k + DEC_WARPS;
     return (ints + 3) / 4 * 4;  // keep what follows 16-byte aligned
 }
@@ -99,68 +103,82 @@ __device__ RouteMap carve_map(int* p, const DecodeShape& s, bool with_w) {
     m.sid = p;
     p += s.B * s.k;
     m.wtot = p;
+    p += DEC_WARPS;
+    m.ucnt = with_w ? p : nullptr;
     return m;
 }
 
 __device__ void build_route_map(const RouteMap& m, const int32_t* __restrict__ ids,
-                                const float* __restrict__ w, const DecodeShape& s, int* err) {
+                                const float* __restrict__ w, const DecodeShape& s, int* err,
+                                bool merge = false) {
+    // The first PT = min(blockDim.x, DEC_THREADS) threads (whole warps) build
+    // the map; any further threads only take part in the barriers.
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int PT = min((int)blockDim.x, DEC_THREADS) & ~31, PW = PT >> 5;
+    const bool part = tid < PT;
     const int n = s.B * s.k;
-    for (int e = tid; e < s.E; e += DEC_THREADS) m.cnt[e] = 0;
+    if (part)
+        for (int e = tid; e < s.E; e += PT) m.cnt[e] = 0;
     __syncthreads();
-    int bad = 0;
-    for (int f = tid; f < n; f += DEC_THREADS) {
-        int e = ids[f];
-        if ((unsigned)e < (unsigned)s.E) {
-            atomicAdd(&m.cnt[e], 1);
-        } else {
-            e = -1;
-            bad = 1;
+    if (part) {
+        int bad = 0;
+        for (int f = tid; f < n; f += PT) {
+            int e = ids[f];
+            if ((unsigned)e < (unsigned)s.E) {
+                atomicAdd(&m.cnt[e], 1);
+            } else {
+                e = -1;
+                bad = 1;
+            }
+            m.sid[f] = e;
         }
-        m.sid[f] = e;
+        if (bad) atomicOr(err, MOE_DEVERR_EXPERT_ID);
     }
-    if (bad) atomicOr(err, MOE_DEVERR_EXPERT_ID);
     __syncthreads();
 
     // Exclusive scan over experts of (count << 16 | present): gives each
     // present expert its distinct index (low half) and slot offset (high).
-    const int per = (s.E + DEC_THREADS - 1) / DEC_THREADS;
-    const int e0 = min(tid * per, s.E), e1 = min(e0 + per, s.E);
-    int local = 0;
-    for (int e = e0; e < e1; ++e) {
-        const int c = m.cnt[e];
-        local += (c << 16) | (c > 0 ? 1 : 0);
+    const int per = (s.E + PT - 1) / PT;
+    const int e0 = part ? min(tid * per, s.E) : s.E, e1 = part ? min(e0 + per, s.E) : s.E;
+    int local = 0, incl = 0;
+    if (part) {
+        for (int e = e0; e < e1; ++e) {
+            const int c = m.cnt[e];
+            local += (c << 16) | (c > 0 ? 1 : 0);
+        }
+        incl = local;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(FULL_MASK, incl, off);
+            if (lane >= off) incl += v;
+        }
+        if (lane == 31) m.wtot[warp] = incl;
     }
-    int incl = local;
-    for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_up_sync(FULL_MASK, incl, off);
-        if (lane >= off) incl += v;
-    }
-    if (lane == 31) m.wtot[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        const int v = lane < DEC_WARPS ? m.wtot[lane] : 0;
+        const int v = lane < PW ? m.wtot[lane] : 0;
         int sc = v;
         for (int off = 1; off < 32; off <<= 1) {
             const int t = __shfl_up_sync(FULL_MASK, sc, off);
             if (lane >= off) sc += t;
         }
-        if (lane < DEC_WARPS) m.wtot[lane] = sc - v;
-        if (lane == DEC_WARPS - 1) {
+        if (lane < PW) m.wtot[lane] = sc - v;
+        if (lane == PW - 1) {
             m.hdr[1] = sc & 0xffff;
             m.hdr[2] = sc >> 16;
         }
     }
     __syncthreads();
-    int run = m.wtot[warp] + incl - local;
-    for (int e = e0; e < e1; ++e) {
-        const int c = m.cnt[e];
-        if (c > 0) {
-            const int uid = run & 0xffff, off = run >> 16;
-            m.uexp[uid] = e;
-            m.uoff[uid] = off;
-            m.cnt[e] = off;
-            run += (c << 16) | 1;
+    if (part) {
+        int run = m.wtot[warp] + incl - local;
+        for (int e = e0; e < e1; ++e) {
+            const int c = m.cnt[e];
+            if (c > 0) {
+                const int uid = run & 0xffff, off = run >> 16;
+                m.uexp[uid] = e;
+                m.uoff[uid] = off;
+                m.cnt[e] = off;
+                run += (c << 16) | 1;
+            }
         }
     }
     __syncthreads();
@@ -194,13 +212,37 @@ __device__ void build_route_map(const RouteMap& m, const int32_t* __restrict__ i
             m.uoff[nu + 1] = tot + s.B;
         }
     }
-    if (s.S) {
-        for (int b = tid; b < s.B; b += DEC_THREADS) {
+    if (s.S && part) {
+        for (int b = tid; b < s.B; b += PT) {
             m.hrow[tot + b] = b * KS + s.k;
             if (m.wt) m.wt[tot + b] = 1.0f;
         }
     }
     __syncthreads();
+    if (merge) {
+        // A token that picked the same expert twice gets one entry with the
+        // summed routing weight (its two h rows are equal); entries of one
+        // token are adjacent because placement follows the flat slot order.
+        const int ntot = m.hdr[0];
+        if (part) {
+            for (int u = tid; u < ntot; u += PT) {
+                const int i0 = m.uoff[u], i1 = m.uoff[u + 1];
+                int wpos = i0;
+                for (int i = i0; i < i1; ++i) {
+                    const int hr = m.hrow[i];
+                    if (wpos > i0 && hr / KS == m.hrow[wpos - 1] / KS) {
+                        m.wt[wpos - 1] += m.wt[i];
+                    } else {
+                        m.hrow[wpos] = hr;
+                        m.wt[wpos] = m.wt[i];
+                        ++wpos;
+                    }
+                }
+                m.ucnt[u] = wpos - i0;
+            }
+        }
+        __syncthreads();
+    }
 }
 
 template <int L>
@@ -316,6 +358,232 @@ __global__ void __launch_bounds__(DEC_THREADS) gate_up_kernel(GateUpArgs a) {
     }
 }
 
+// --------------------------------------------------------- gate/up v2 ----
+// Each warp owns (distinct expert, pair of rows) items.  A lane handles
+// 16-byte K chunks (16 E4M3 codes, all inside one 32-element scale block) of
+// both rows and both projections, so one BF16->FP32 conversion of x serves
+// four weight rows.  Chunks are prefetched into a per-warp shared-memory ring
+// with cp.async (each lane reads back only the bytes it copied, so no warp
+// barrier is needed); x comes through L1, where the CTA's warps, which walk
+// adjacent rows of the same expert, share it.  The E8M0 scale multiplies each
+// chunk's partial sums once; the 4 x NT results of an item are reduced across
+// the warp in one reduce-scatter.  Needs d % 128 == 0 (4-byte scale words).
+
+constexpr int GU2_STAGES = 4;
+constexpr int GU2_PARTS = 4;  // (row 0 gate, row 1 gate, row 0 up, row 1 up)
+constexpr int GU2_CHUNK = 512;  // K bytes per warp per part per step (32 lanes x 16)
+
+struct GU2Ring {
+    uint4 w[GU2_STAGES][GU2_PARTS][32];
+    uint32_t s[GU2_STAGES][GU2_PARTS][32];
+};
+
+struct GU2Warp {
+    int first, stride, end;  // this warp's items: first, first + stride, ... < end
+    int tiles;               // row pairs per expert
+    int nch;                 // chunks per row
+};
+
+struct GU2Cursor {
+    int m, g, c;  // item ordinal of this warp, token group, chunk
+};
+
+__device__ __forceinline__ int gu2_groups(const RouteMap& m, int u) {
+    return (m.uoff[u + 1] - m.uoff[u] + TC - 1) / TC;
+}
+
+// Issue the copies of the step under the cursor into ring slot `slot` and
+// advance the cursor; always commits one group (empty past the end).
+__device__ __forceinline__ void gu2_issue(const GateUpArgs& a, const RouteMap& m, const GU2Warp& wi,
+                                          GU2Cursor& pc, GU2Ring* ring, int slot, int lane,
+                                          uint64_t pol) {
+    const int item = wi.first + pc.m * wi.stride;
+    if (item < wi.end) {
+        const DecodeShape& s = a.s;
+        const int u = item / wi.tiles;
+        const int n0 = (item - u * wi.tiles) * 2;
+        const int e = m.uexp[u];
+        const bool sh = e >= s.E;
+        const size_t eo = sh ? 0 : (size_t)e;
+        const MXView vg = sh ? a.shg : a.wg, vu = sh ? a.shu : a.wu;
+        const size_t r0 = eo * s.I + n0;
+        const int kofs = pc.c * GU2_CHUNK + lane * 16;
+        const bool ok = kofs < s.d;
+        const int kk = ok ? kofs : 0;
+        const int nb = s.d / 32;
+        const int sw = ok ? (((pc.c * 16 + (lane >> 1)) >> 2) << 2) : 0;
+        const uint8_t* wrow[GU2_PARTS] = {vg.w + r0 * s.d, vg.w + (r0 + 1) * s.d, vu.w + r0 * s.d,
+                                          vu.w + (r0 + 1) * s.d};
+        const uint8_t* srow[GU2_PARTS] = {vg.s + r0 * nb, vg.s + (r0 + 1) * nb, vu.s + r0 * nb,
+                                          vu.s + (r0 + 1) * nb};
+#pragma unroll
+        for (int p = 0; p < GU2_PARTS; ++p) {
+            cp_async_16(&ring->w[slot][p][lane], wrow[p] + kk, ok ? 16 : 0, pol);
+            cp_async_4(&ring->s[slot][p][lane], srow[p] + sw, ok ? 4 : 0);
+        }
+        if (++pc.c == wi.nch) {
+            pc.c = 0;
+            if (++pc.g == gu2_groups(m, u)) {
+                pc.g = 0;
+                ++pc.m;
+            }
+        }
+    }
+    cp_async_commit();
+}
+
+template <int NT, bool FOLD>
+__device__ __forceinline__ void gu2_group(const GateUpArgs& a, const RouteMap& m, const GU2Warp& wi,
+                                          GU2Cursor& pc, GU2Ring* ring, int& slot, int lane,
+                                          uint64_t pol, int n0, const int* hs, int nt) {
+    constexpr int NTP = NT == 3 ? 4 : NT;  // padded to a power of two for the reduction
+    const DecodeShape& s = a.s;
+    const int KS = s.k + s.S;
+    const char* xr[NT];
+    int hr[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        hr[t] = hs[t];
+        xr[t] = reinterpret_cast<const char*>(a.x + (size_t)(hr[t] / KS) * s.d);
+    }
+    float2 acc[GU2_PARTS][NT];
+#pragma unroll
+    for (int p = 0; p < GU2_PARTS; ++p)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[p][t] = make_float2(0.f, 0.f);
+    const int bsh = ((lane >> 1) & 3) * 8;  // this lane's scale byte inside its 4-byte word
+
+    for (int c = 0; c < wi.nch; ++c) {
+        gu2_issue(a, m, wi, pc, ring, (slot + GU2_STAGES - 1) % GU2_STAGES, lane, pol);
+        cp_async_wait<GU2_STAGES - 1>();
+        const int kofs = c * GU2_CHUNK + lane * 16;
+        const bool kin = kofs < s.d;
+        uint4 wv[GU2_PARTS];
+        float sc[GU2_PARTS];
+#pragma unroll
+        for (int p = 0; p < GU2_PARTS; ++p) {
+            wv[p] = ring->w[slot][p][lane];
+            sc[p] = e8m0_to_float((ring->s[slot][p][lane] >> bsh) & 0xffu);
+        }
+        float2 part[GU2_PARTS][NT];
+#pragma unroll
+        for (int p = 0; p < GU2_PARTS; ++p)
+#pragma unroll
+            for (int t = 0; t < NT; ++t) part[p][t] = make_float2(0.f, 0.f);
+        uint4 xv[NT];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {  // pairs of K elements
+            if ((q & 3) == 0) {        // next 8 activations of every token
+#pragma unroll
+                for (int t = 0; t < NT; ++t)
+                    xv[t] = kin ? ld_cached_128(xr[t] + (size_t)kofs * 2 + (q >> 2) * 16) : make_uint4(0, 0, 0, 0);
+            }
+            float2 wq[GU2_PARTS];
+#pragma unroll
+            for (int p = 0; p < GU2_PARTS; ++p) {
+                const uint32_t word = (&wv[p].x)[q >> 1];
+                wq[p] = e4m3x2_to_float2(word >> ((q & 1) * 16));
+                if (!FOLD) wq[p] = __fmul2_rn(wq[p], make_float2(sc[p], sc[p]));
+            }
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const uint32_t xw = (&xv[t].x)[q & 3];
+                const float2 xf = bf16x2_to_float2(xw);
+#pragma unroll
+                for (int p = 0; p < GU2_PARTS; ++p) {
+                    if (FOLD)
+                        part[p][t] = __ffma2_rn(xf, wq[p], part[p][t]);
+                    else
+                        acc[p][t] = __ffma2_rn(xf, wq[p], acc[p][t]);
+                }
+            }
+        }
+        if (FOLD) {
+#pragma unroll
+            for (int p = 0; p < GU2_PARTS; ++p)
+#pragma unroll
+                for (int t = 0; t < NT; ++t)
+                    acc[p][t] = __ffma2_rn(part[p][t], make_float2(sc[p], sc[p]), acc[p][t]);
+        }
+        slot = (slot + 1) % GU2_STAGES;
+    }
+
+    // value index = proj * 2NTP + row * NTP + token
+    constexpr int N = 4 * NTP;
+    float v[N];
+#pragma unroll
+    for (int p = 0; p < GU2_PARTS; ++p) {
+        const int proj = p >> 1, rr = p & 1;
+#pragma unroll
+        for (int t = 0; t < NTP; ++t)
+            v[proj * 2 * NTP + rr * NTP + t] = t < NT ? acc[p][t < NT ? t : 0].x + acc[p][t < NT ? t : 0].y : 0.f;
+    }
+    const float r = warp_reduce_scatter<N>(v, lane);
+    const float up = __shfl_xor_sync(FULL_MASK, r, 16);
+    constexpr int LOGN = N == 4 ? 2 : (N == 8 ? 3 : 4);
+    const int idx = (lane >> (5 - LOGN)) & (N - 1);
+    const int proj = idx / (2 * NTP), rr = (idx / NTP) & 1, t = idx % NTP;
+    const bool lead = (lane & ((1 << (5 - LOGN)) - 1)) == 0;
+    if (proj == 0 && lead && t < nt) {
+        const float hv = r / (1.0f + expf(-r)) * up;
+        int hrow = hs[0];
+#pragma unroll
+        for (int tt = 1; tt < NT; ++tt)
+            if (tt == t) hrow = hr[tt];
+        a.h[(size_t)hrow * s.I + n0 + rr] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+    }
+}
+
+#ifndef MOEDEC_GU2_MINB
+#define MOEDEC_GU2_MINB 2
+#endif
+
+template <bool FOLD>
+__global__ void __launch_bounds__(DEC_THREADS, MOEDEC_GU2_MINB) gate_up_v2_kernel(GateUpArgs a) {
+    extern __shared__ __align__(16) int smem_i[];
+    const DecodeShape s = a.s;
+    const RouteMap m = carve_map(smem_i, s, false);
+    GU2Ring* rings = reinterpret_cast<GU2Ring*>(smem_i + map_ints(s, false));
+    build_route_map(m, a.ids, nullptr, s, a.err);
+    asm volatile("griddepcontrol.launch_dependents;");
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    GU2Ring* ring = rings + warp;
+    const int nu = m.hdr[0];
+    GU2Warp wi;
+    wi.tiles = s.I / 2;
+    wi.nch = (s.d + GU2_CHUNK - 1) / GU2_CHUNK;
+    // items round-robin over every warp of the grid: consecutive items (rows
+    // of one expert) run at the same time on the warps of one CTA, and a hot
+    // expert's items spread over the whole GPU
+    wi.end = nu * wi.tiles;
+    wi.first = blockIdx.x * DEC_WARPS + warp;
+    wi.stride = gridDim.x * DEC_WARPS;
+    const uint64_t pol = l2_evict_first_policy();
+
+    GU2Cursor pc{0, 0, 0};
+    int slot = 0;
+#pragma unroll
+    for (int i = 0; i < GU2_STAGES - 1; ++i) gu2_issue(a, m, wi, pc, ring, i, lane, pol);
+
+    for (int item = wi.first; item < wi.end; item += wi.stride) {
+        const int u = item / wi.tiles;
+        const int n0 = (item - u * wi.tiles) * 2;
+        const int s0 = m.uoff[u], s1 = m.uoff[u + 1];
+        for (int t0 = s0; t0 < s1; t0 += TC) {
+            const int nt = min(TC, s1 - t0);
+            const int* hs = m.hrow + t0;
+            switch (nt) {
+                case 1: gu2_group<1, FOLD>(a, m, wi, pc, ring, slot, lane, pol, n0, hs, nt); break;
+                case 2: gu2_group<2, FOLD>(a, m, wi, pc, ring, slot, lane, pol, n0, hs, nt); break;
+                case 3: gu2_group<3, FOLD>(a, m, wi, pc, ring, slot, lane, pol, n0, hs, nt); break;
+                default: gu2_group<4, FOLD>(a, m, wi, pc, ring, slot, lane, pol, n0, hs, nt); break;
+            }
+        }
+    }
+    cp_async_wait<0>();
+}
+
 // --------------------------------------------------------------- down ----
 
 template <int L, int NT>
@@ -420,6 +688,715 @@ __global__ void __launch_bounds__(DEC_THREADS) down_kernel(DownArgs a) {
     }
 }
 
+// --------------------------------------------------------- gate/up v3 ----
+// Warp-specialised: one producer warp streams, per stage, a 16-row x 512-byte
+// K slice of the gate and up weights of one distinct expert (one 1D bulk
+// copy per row and projection, plus the matching E8M0 scale bytes) and the
+// same K slice of x for up to TC tokens into a 4-stage shared-memory ring,
+// completion counted on an mbarrier; eight consumer warps each own two of the
+// 16 rows, lanes take 16 bytes of the slice, and compute as in v2.  A tile =
+// (distinct expert, 16 rows); tiles are dealt round-robin to persistent CTAs,
+// and a tile with more than TC tokens streams its slices once per token
+// group (the repeat hits L2).  Every wait is bounded.  Needs d % 512 == 0.
+
+constexpr int GU3_CW = 8;                       // consumer warps
+constexpr int GU3_THREADS = (GU3_CW + 1) * 32;  // + one producer warp
+constexpr int GU3_ROWS = 2 * GU3_CW;            // weight rows per tile
+constexpr int GU3_KT = 512;                     // K bytes per stage
+constexpr int GU3_S = 4;                        // ring stages
+#ifndef MOEDEC_GU3_MINB
+#define MOEDEC_GU3_MINB 2
+#endif
+#ifndef MOEDEC_GU3_FOLD
+#define MOEDEC_GU3_FOLD 0
+#endif
+
+constexpr int GU3_BOX = 256;                    // inner box of a 2D tensor copy (bytes)
+
+struct __align__(128) GU3Stage {
+    uint8_t w[2][GU3_KT / GU3_BOX][GU3_ROWS][GU3_BOX];  // [proj][half][row][k]
+    uint8_t sc[2][GU3_ROWS][16];                        // E8M0 scales of the slice
+    uint16_t x[TC][GU3_KT];                             // BF16 activations of the slice
+};
+
+struct GU3Smem {
+    GU3Stage st[GU3_S];
+    uint64_t full[GU3_S];
+    uint64_t empty[GU3_S];
+};
+
+// 2D tensor maps (uint8, [rows][cols]) of the weight codes and scales.
+struct GU3Maps {
+    CUtensorMap w[2][2];  // [routed / shared][gate / up], box 16 rows x 256 B
+    CUtensorMap s[2][2];  // the same for the scales, box 16 rows x 16 B
+};
+
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                       uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(pol)
+        : "memory");
+}
+
+template <int NT>
+__device__ __forceinline__ bool gu3_group(const GateUpArgs& a, GU3Smem* sm, uint32_t& it, int nkt,
+                                          int cw, int lane, int n0, const int* hs, int nt) {
+    constexpr int NTP = NT == 3 ? 4 : NT;
+    const DecodeShape& s = a.s;
+    float2 acc[GU2_PARTS][NT];
+#pragma unroll
+    for (int p = 0; p < GU2_PARTS; ++p)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[p][t] = make_float2(0.f, 0.f);
+
+    for (int kt = 0; kt < nkt; ++kt, ++it) {
+        const int slot = it % GU3_S;
+        if (!mbar_wait(&sm->full[slot], (it / GU3_S) & 1)) return false;
+        const GU3Stage& st = sm->st[slot];
+        uint4 wv[GU2_PARTS];
+        float sc[GU2_PARTS];
+#pragma unroll
+        for (int p = 0; p < GU2_PARTS; ++p) {  // part = proj * 2 + row
+            const int proj = p >> 1, row = 2 * cw + (p & 1);
+            wv[p] = *reinterpret_cast<const uint4*>(&st.w[proj][lane >> 4][row][(lane & 15) * 16]);
+            sc[p] = e8m0_to_float(st.sc[proj][row][lane >> 1]);
+        }
+#if MOEDEC_GU3_FOLD
+        float2 part[GU2_PARTS][NT];
+#endif
+        uint4 xv[NT];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {  // groups of four K elements
+            if ((q4 & 1) == 0) {
+#pragma unroll
+                for (int t = 0; t < NT; ++t)
+                    xv[t] = *reinterpret_cast<const uint4*>(&st.x[t][lane * 16 + (q4 >> 1) * 8]);
+            }
+            float2 wq[GU2_PARTS][2];
+#pragma unroll
+            for (int p = 0; p < GU2_PARTS; ++p) {
+                e4m3x4_to_float((&wv[p].x)[q4], wq[p][0], wq[p][1]);
+#if !MOEDEC_GU3_FOLD
+                wq[p][0] = __fmul2_rn(wq[p][0], make_float2(sc[p], sc[p]));
+                wq[p][1] = __fmul2_rn(wq[p][1], make_float2(sc[p], sc[p]));
+#endif
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    const float2 xf = bf16x2_to_float2((&xv[t].x)[(q4 & 1) * 2 + h]);
+#pragma unroll
+                    for (int p = 0; p < GU2_PARTS; ++p) {
+#if MOEDEC_GU3_FOLD
+                        if (q4 == 0 && h == 0)
+                            part[p][t] = __fmul2_rn(xf, wq[p][h]);
+                        else
+                            part[p][t] = __ffma2_rn(xf, wq[p][h], part[p][t]);
+#else
+                        acc[p][t] = __ffma2_rn(xf, wq[p][h], acc[p][t]);
+#endif
+                    }
+                }
+            }
+        }
+#if MOEDEC_GU3_FOLD
+#pragma unroll
+        for (int p = 0; p < GU2_PARTS; ++p)
+#pragma unroll
+            for (int t = 0; t < NT; ++t) acc[p][t] = __ffma2_rn(part[p][t], make_float2(sc[p], sc[p]), acc[p][t]);
+#endif
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->empty[slot]);
+    }
+
+    constexpr int N = 4 * NTP;  // value index = proj * 2NTP + row * NTP + token
+    float v[N];
+#pragma unroll
+    for (int p = 0; p < GU2_PARTS; ++p) {
+        const int proj = p >> 1, rr = p & 1;
+#pragma unroll
+        for (int t = 0; t < NTP; ++t)
+            v[proj * 2 * NTP + rr * NTP + t] = t < NT ? acc[p][t < NT ? t : 0].x + acc[p][t < NT ? t : 0].y : 0.f;
+    }
+    const float r = warp_reduce_scatter<N>(v, lane);
+    const float up = __shfl_xor_sync(FULL_MASK, r, 16);
+    constexpr int LOGN = N == 4 ? 2 : (N == 8 ? 3 : 4);
+    const int idx = (lane >> (5 - LOGN)) & (N - 1);
+    const int proj = idx / (2 * NTP), rr = (idx / NTP) & 1, t = idx % NTP;
+    const bool lead = (lane & ((1 << (5 - LOGN)) - 1)) == 0;
+    if (proj == 0 && lead && t < nt) {
+        const float hv = r / (1.0f + expf(-r)) * up;
+        int hrow = hs[0];
+#pragma unroll
+        for (int tt = 1; tt < NT; ++tt)
+            if (tt == t) hrow = hs[tt];
+        a.h[(size_t)hrow * s.I + n0 + 2 * cw + rr] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+    }
+    return true;
+}
+
+__host__ __device__ inline size_t gu3_smem_offset(const DecodeShape& s) {
+    return (map_ints(s, false) * 4 + 127) / 128 * 128;
+}
+
+__global__ void __launch_bounds__(GU3_THREADS, MOEDEC_GU3_MINB)
+    gate_up_v3_kernel(GateUpArgs a, const __grid_constant__ GU3Maps maps) {
+    extern __shared__ __align__(128) int smem_i[];
+    const DecodeShape s = a.s;
+    const RouteMap m = carve_map(smem_i, s, false);
+    // tensor copies want 128-byte aligned destinations: align at run time
+    // (the launch reserves 128 spare bytes)
+    const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_i) + gu3_smem_offset(s);
+    GU3Smem* sm = reinterpret_cast<GU3Smem*>((raw + 127) & ~uintptr_t(127));
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < GU3_S; ++i) {
+            mbar_init(&sm->full[i], 1);
+            mbar_init(&sm->empty[i], GU3_CW);
+        }
+        mbar_init_fence();
+    }
+    build_route_map(m, a.ids, nullptr, s, a.err);  // ends with __syncthreads
+    asm volatile("griddepcontrol.launch_dependents;");
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int KS = s.k + s.S;
+    const int rbs = s.I / GU3_ROWS;
+    const int tiles = m.hdr[0] * rbs;
+    const int nkt = s.d / GU3_KT;
+    bool ok = true;
+    uint32_t it = 0;  // stages produced / consumed by this thread so far
+
+    if (warp == GU3_CW) {
+        // ---------------- producer ----------------
+        const uint64_t pol = l2_evict_first_policy();
+        for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+            const int u = tile / rbs;
+            const int n0 = (tile - u * rbs) * GU3_ROWS;
+            const int e = m.uexp[u];
+            const int sh = e >= s.E ? 1 : 0;
+            const int row0 = (sh ? 0 : e) * s.I + n0;
+            const int s0 = m.uoff[u], s1 = m.uoff[u + 1];
+            for (int t0 = s0; t0 < s1 && ok; t0 += TC) {
+                const int nt = min(TC, s1 - t0);
+                const uint16_t* xrow = a.x + (size_t)(lane < nt ? m.hrow[t0 + lane] / KS : 0) * s.d;
+                for (int kt = 0; kt < nkt; ++kt, ++it) {
+                    const int slot = it % GU3_S;
+                    if (it >= GU3_S && !mbar_wait(&sm->empty[slot], ((it / GU3_S) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    GU3Stage& st = sm->st[slot];
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&sm->full[slot],
+                                              2 * GU3_ROWS * (GU3_KT + 16) + nt * GU3_KT * 2);
+                        fence_proxy_async();
+#pragma unroll
+                        for (int p = 0; p < 2; ++p) {
+#pragma unroll
+                            for (int hf = 0; hf < GU3_KT / GU3_BOX; ++hf)
+                                tma_2d(st.w[p][hf], &maps.w[sh][p], kt * GU3_KT + hf * GU3_BOX, row0,
+                                       &sm->full[slot], pol);
+                            tma_2d(st.sc[p], &maps.s[sh][p], kt * 16, row0, &sm->full[slot], pol);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane < nt) {
+                        fence_proxy_async();
+                        bulk_g2s_keep(st.x[lane], xrow + (size_t)kt * GU3_KT, GU3_KT * 2, &sm->full[slot]);
+                    }
+                }
+            }
+        }
+        // never leave the CTA with a copy in flight: wait for the last stages
+        for (uint32_t j = it > GU3_S ? it - GU3_S : 0; j < it; ++j)
+            mbar_wait(&sm->full[j % GU3_S], (j / GU3_S) & 1);
+    } else {
+        // ---------------- consumers ----------------
+        for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+            const int u = tile / rbs;
+            const int n0 = (tile - u * rbs) * GU3_ROWS;
+            const int s0 = m.uoff[u], s1 = m.uoff[u + 1];
+            for (int t0 = s0; t0 < s1 && ok; t0 += TC) {
+                const int nt = min(TC, s1 - t0);
+                const int* hs = m.hrow + t0;
+                switch (nt) {
+                    case 1: ok = gu3_group<1>(a, sm, it, nkt, warp, lane, n0, hs, nt); break;
+                    case 2: ok = gu3_group<2>(a, sm, it, nkt, warp, lane, n0, hs, nt); break;
+                    case 3: ok = gu3_group<3>(a, sm, it, nkt, warp, lane, n0, hs, nt); break;
+                    default: ok = gu3_group<4>(a, sm, it, nkt, warp, lane, n0, hs, nt); break;
+                }
+            }
+        }
+    }
+    if (!ok && lane == 0) atomicOr(a.err, MOE_DEVERR_TIMEOUT);
+}
+
+// ------------------------------------------------------------ down v2 ----
+// The CTA owns RT output rows and keeps one FP32 accumulator per (row,
+// token) in shared memory.  Its warps split the rows and the distinct
+// experts; a lane group of L lanes covers L x 16 bytes of I per step for two
+// rows at once (one h load serves both).  Weight chunks stream through a
+// per-warp cp.async ring; the first ones are issued before waiting for the
+// gate/up pass, since they do not depend on it.  After each (expert, token
+// group) a reduce-scatter inside the lane group leaves each (row, token)
+// dot in one lane, which adds w * dot to the accumulator.  Needs I % 128 == 0.
+
+constexpr int DN2_STAGES = 4;
+constexpr int DN2_R = 2;  // rows per lane
+
+struct DN2Ring {
+    uint4 w[DN2_STAGES][DN2_R][32];
+    uint32_t s[DN2_STAGES][DN2_R][32];
+};
+
+struct DN2Warp {
+    int es, ES, nu, nstep, rbase;
+};
+
+template <int N, int L>
+__device__ __forceinline__ float group_reduce_scatter(float (&v)[N], int li) {
+    int o = L / 2;
+#pragma unroll
+    for (int cnt = N; cnt > 1; cnt >>= 1, o >>= 1) {
+        const bool upper = (li & o) != 0;
+#pragma unroll
+        for (int i = 0; i < cnt / 2; ++i) {
+            const float send = upper ? v[i] : v[i + cnt / 2];
+            const float keep = upper ? v[i + cnt / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(FULL_MASK, send, o);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (; o >= 1; o >>= 1) r += __shfl_xor_sync(FULL_MASK, r, o);
+    return r;
+}
+
+template <int L>
+__device__ __forceinline__ void dn2_issue(const DownArgs& a, const RouteMap& m, const DN2Warp& wi,
+                                          GU2Cursor& pc, DN2Ring* ring, int slot, int lane,
+                                          uint64_t pol) {
+    const int u = wi.es + pc.m * wi.ES;
+    if (u < wi.nu) {
+        const DecodeShape& s = a.s;
+        const int e = m.uexp[u];
+        const bool sh = e >= s.E;
+        const MXView vd = sh ? a.shd : a.wd;
+        const size_t eo = sh ? 0 : (size_t)e;
+        const int kofs = pc.c * (L * 16) + (lane % L) * 16;
+        const int nb = s.I / 32;
+        const int sw = ((kofs >> 5) >> 2) << 2;
+#pragma unroll
+        for (int rr = 0; rr < DN2_R; ++rr) {
+            const int row = min(wi.rbase + rr, s.d - 1);
+            const size_t r = eo * s.d + row;
+            cp_async_16(&ring->w[slot][rr][lane], vd.w + r * s.I + kofs, 16, pol);
+            cp_async_4(&ring->s[slot][rr][lane], vd.s + r * nb + sw, 4);
+        }
+        if (++pc.c == wi.nstep) {
+            pc.c = 0;
+            if (++pc.g == (m.ucnt[u] + TC - 1) / TC) {
+                pc.g = 0;
+                ++pc.m;
+            }
+        }
+    }
+    cp_async_commit();
+}
+
+template <int L, int NT>
+__device__ __forceinline__ void dn2_group(const DownArgs& a, const RouteMap& m, const DN2Warp& wi,
+                                          GU2Cursor& pc, DN2Ring* ring, int& slot, int lane,
+                                          uint64_t pol, const int* hs, const float* ws, int nt,
+                                          float* acc_rows, int RT) {
+    constexpr int NTP = NT == 3 ? 4 : NT;
+    const DecodeShape& s = a.s;
+    const int KS = s.k + s.S;
+    const int li = lane % L;
+    const char* hp[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) hp[t] = reinterpret_cast<const char*>(a.h + (size_t)hs[t] * s.I);
+    float2 acc[DN2_R][NT];
+#pragma unroll
+    for (int r = 0; r < DN2_R; ++r)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[r][t] = make_float2(0.f, 0.f);
+    const int bsh = ((li >> 1) & 3) * 8;
+
+    for (int c = 0; c < wi.nstep; ++c) {
+        dn2_issue<L>(a, m, wi, pc, ring, (slot + DN2_STAGES - 1) % DN2_STAGES, lane, pol);
+        cp_async_wait<DN2_STAGES - 1>();
+        const int kofs = c * (L * 16) + li * 16;
+        uint4 wv[DN2_R];
+        float sc[DN2_R];
+#pragma unroll
+        for (int r = 0; r < DN2_R; ++r) {
+            wv[r] = ring->w[slot][r][lane];
+            sc[r] = e8m0_to_float((ring->s[slot][r][lane] >> bsh) & 0xffu);
+        }
+        uint4 hv[NT];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            if ((q & 3) == 0) {
+#pragma unroll
+                for (int t = 0; t < NT; ++t) hv[t] = ld_cached_128(hp[t] + (size_t)kofs * 2 + (q >> 2) * 16);
+            }
+            float2 wq[DN2_R];
+#pragma unroll
+            for (int r = 0; r < DN2_R; ++r)
+                wq[r] = __fmul2_rn(e4m3x2_to_float2((&wv[r].x)[q >> 1] >> ((q & 1) * 16)),
+                                   make_float2(sc[r], sc[r]));
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const float2 hf = bf16x2_to_float2((&hv[t].x)[q & 3]);
+#pragma unroll
+                for (int r = 0; r < DN2_R; ++r) acc[r][t] = __ffma2_rn(hf, wq[r], acc[r][t]);
+            }
+        }
+        slot = (slot + 1) % DN2_STAGES;
+    }
+    constexpr int N = DN2_R * NTP;  // value index = row * NTP + token
+    float v[N];
+#pragma unroll
+    for (int r = 0; r < DN2_R; ++r)
+#pragma unroll
+        for (int t = 0; t < NTP; ++t)
+            v[r * NTP + t] = t < NT ? acc[r][t < NT ? t : 0].x + acc[r][t < NT ? t : 0].y : 0.f;
+    const float dot = group_reduce_scatter<N, L>(v, li);
+    constexpr int LOGN = N == 2 ? 1 : (N == 4 ? 2 : 3);
+    constexpr int LOGL = L == 8 ? 3 : (L == 16 ? 4 : 5);
+    const int idx = (li >> (LOGL - LOGN)) & (N - 1);
+    const int rr = idx / NTP, t = idx % NTP;
+    if ((li & ((1 << (LOGL - LOGN)) - 1)) == 0 && t < nt && wi.rbase + rr < s.d) {
+        int hrow = hs[0];
+        float wt = ws[0];
+#pragma unroll
+        for (int tt = 1; tt < NT; ++tt)
+            if (tt == t) {
+                hrow = hs[tt];
+                wt = ws[tt];
+            }
+        acc_rows[rr * s.B + hrow / KS] += wt * dot;
+    }
+}
+
+template <int L>
+__global__ void __launch_bounds__(DEC_THREADS, 2) down_v2_kernel(DownArgs a) {
+    extern __shared__ __align__(16) int smem_i[];
+    const DecodeShape s = a.s;
+    const RouteMap m = carve_map(smem_i, s, true);
+    constexpr int G = 32 / L;
+    const int RS = DEC_WARPS / a.es;
+    const int RT = RS * G * DN2_R;
+    float* acc = reinterpret_cast<float*>(smem_i + map_ints(s, true));
+    const int acc_n = DEC_WARPS * G * DN2_R * s.B;  // = ES * RT * B
+    DN2Ring* rings = reinterpret_cast<DN2Ring*>(acc + (acc_n + 3) / 4 * 4);
+    build_route_map(m, a.ids, a.w, s, a.err, true);
+    for (int i = threadIdx.x; i < acc_n; i += DEC_THREADS) acc[i] = 0.f;
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int grp = lane / L;
+    const int rs = warp % RS, es = warp / RS;
+    DN2Warp wi;
+    wi.es = es;
+    wi.ES = a.es;
+    wi.nu = m.hdr[0];
+    wi.nstep = s.I / (L * 16);
+    const int rloc = (rs * G + grp) * DN2_R;
+    wi.rbase = blockIdx.x * RT + rloc;
+    DN2Ring* ring = rings + warp;
+    const uint64_t pol = l2_evict_first_policy();
+    GU2Cursor pc{0, 0, 0};
+    int slot = 0;
+    // weight prefetch does not depend on the gate/up pass
+#pragma unroll
+    for (int i = 0; i < DN2_STAGES - 1; ++i) dn2_issue<L>(a, m, wi, pc, ring, i, lane, pol);
+    __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    float* acc_rows = acc + (size_t)(es * RT + rloc) * s.B;
+    for (int u = es; u < wi.nu; u += a.es) {
+        const int s0 = m.uoff[u], cnt = m.ucnt[u];
+        for (int t0 = 0; t0 < cnt; t0 += TC) {
+            const int nt = min(TC, cnt - t0);
+            const int* hs = m.hrow + s0 + t0;
+            const float* ws = m.wt + s0 + t0;
+            switch (nt) {
+                case 1: dn2_group<L, 1>(a, m, wi, pc, ring, slot, lane, pol, hs, ws, nt, acc_rows, RT); break;
+                case 2: dn2_group<L, 2>(a, m, wi, pc, ring, slot, lane, pol, hs, ws, nt, acc_rows, RT); break;
+                case 3: dn2_group<L, 3>(a, m, wi, pc, ring, slot, lane, pol, hs, ws, nt, acc_rows, RT); break;
+                default: dn2_group<L, 4>(a, m, wi, pc, ring, slot, lane, pol, hs, ws, nt, acc_rows, RT); break;
+            }
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    for (int i = threadIdx.x; i < RT * s.B; i += DEC_THREADS) {
+        const int r = i % RT, b = i / RT;
+        const int oo = blockIdx.x * RT + r;
+        if (oo < s.d) {
+            float sum = 0.f;
+            for (int q = 0; q < a.es; ++q) sum += acc[(size_t)(q * RT + r) * s.B + b];
+            a.y[(size_t)b * s.d + oo] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+        }
+    }
+}
+
+// ------------------------------------------------------------ down v3 ----
+// Warp-specialised like gate/up v3.  A CTA owns DN3_RT = 8 output rows; the
+// stages are the (distinct expert, group of up to TC tokens) pairs in order,
+// and stage j holds the expert's contiguous [8 rows x I] block of Wd, its
+// scale block and the tokens' h rows, brought in by three kinds of 1D bulk
+// copies (the weight copies of the first stages go out before waiting for
+// the gate/up pass).  Eight consumer warps form RW expert splits of 8/RW
+// warps; split j % RW takes stage j, each of its warps owning RW rows (one h
+// load serves RW rows), lanes taking 8-byte K chunks (eight E4M3 codes in
+// one scale block, whose partial sums are scaled once).  Each split has its
+// own ring slots, so every barrier phase is consumed in order.  After each
+// stage a reduce-scatter leaves each (row, token) dot in one lane, which adds
+// w * dot to the split's FP32 accumulator in shared memory; the splits are
+// added in a fixed order at the end.  Needs I % 256 == 0.
+
+constexpr int DN3_CW = 8;                       // consumer warps
+constexpr int DN3_THREADS = (DN3_CW + 1) * 32;  // + producer warp
+constexpr int DN3_RT = 8;                       // rows per CTA
+constexpr int DN3_SMAX = 8;                     // ring slots (all splits)
+constexpr int DN3_RING_BYTES = 80 * 1024;  // two CTAs per SM
+
+struct DN3Layout {
+    int stage_bytes, w_off, s_off, h_off, S;  // S = slots per split
+};
+
+__host__ __device__ inline DN3Layout dn3_layout(const DecodeShape& s, int RW) {
+    DN3Layout L;
+    L.w_off = 0;
+    L.s_off = DN3_RT * s.I;  // multiple of 16
+    L.h_off = (L.s_off + DN3_RT * (s.I / 32) + 127) / 128 * 128;
+    L.stage_bytes = (L.h_off + TC * s.I * 2 + 127) / 128 * 128;
+    int S = DN3_RING_BYTES / (RW * L.stage_bytes);
+    const int smax = DN3_SMAX / RW;
+    L.S = S > smax ? smax : S;  // >= 2 is checked by the launcher
+    return L;
+}
+
+__host__ __device__ inline size_t dn3_smem_offset(const DecodeShape& s, int RW) {
+    const size_t acc = (size_t)RW * DN3_RT * s.B * 4;
+    return (map_ints(s, true) * 4 + acc + 127) / 128 * 128;
+}
+
+// Rows per warp (= expert splits) for a given I: at least ~48 weight bytes
+// per lane per stage, and at least two ring slots per split.
+__host__ __device__ inline int dn3_rw(int I) { return I >= 2048 ? 1 : 2; }
+
+template <int RW, int NT>
+__device__ __forceinline__ bool dn3_group(const DownArgs& a, const DN3Layout& L, const char* st, uint64_t* full,
+                                          uint64_t* empty, uint32_t parity, int cw, int lane, const int* hs,
+                                          const float* ws, int nt, float* acc_rows) {
+    constexpr int NTP = NT == 3 ? 4 : NT;
+    const DecodeShape& s = a.s;
+    const int KS = s.k + s.S;
+    if (!mbar_wait(full, parity)) return false;
+    const uint8_t* wb = reinterpret_cast<const uint8_t*>(st + L.w_off);
+    const uint8_t* sb = reinterpret_cast<const uint8_t*>(st + L.s_off);
+    const uint16_t* hb = reinterpret_cast<const uint16_t*>(st + L.h_off);
+    float2 acc[RW][NT];
+#pragma unroll
+    for (int r = 0; r < RW; ++r)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[r][t] = make_float2(0.f, 0.f);
+    const int nch = s.I / 256;  // 8-byte chunks per lane
+    for (int i = 0; i < nch; ++i) {
+        const int k0 = (lane + 32 * i) * 8;  // first K element of this chunk
+        uint4 hv[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) hv[t] = *reinterpret_cast<const uint4*>(hb + (size_t)t * s.I + k0);
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            const int row = cw * RW + r;
+            const uint2 wv = *reinterpret_cast<const uint2*>(wb + (size_t)row * s.I + k0);
+            const float sc = e8m0_to_float(sb[row * (s.I / 32) + (k0 >> 5)]);
+            float2 wq[4];
+            e4m3x4_to_float(wv.x, wq[0], wq[1]);
+            e4m3x4_to_float(wv.y, wq[2], wq[3]);
+            // the chunk lies inside one scale block: scale its partial sum once
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                float2 part = __fmul2_rn(bf16x2_to_float2(hv[t].x), wq[0]);
+#pragma unroll
+                for (int q = 1; q < 4; ++q) part = __ffma2_rn(bf16x2_to_float2((&hv[t].x)[q]), wq[q], part);
+                acc[r][t] = __ffma2_rn(part, make_float2(sc, sc), acc[r][t]);
+            }
+        }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty);
+
+    constexpr int N = RW * NTP;  // value index = row * NTP + token
+    float v[N];
+#pragma unroll
+    for (int r = 0; r < RW; ++r)
+#pragma unroll
+        for (int t = 0; t < NTP; ++t)
+            v[r * NTP + t] = t < NT ? acc[r][t < NT ? t : 0].x + acc[r][t < NT ? t : 0].y : 0.f;
+    const float dot = warp_reduce_scatter<N>(v, lane);
+    constexpr int LOGN = N == 1 ? 0 : (N == 2 ? 1 : (N == 4 ? 2 : (N == 8 ? 3 : 4)));
+    const int idx = (lane >> (5 - LOGN)) & (N - 1);
+    const int rr = idx / NTP, t = idx % NTP;
+    if ((lane & ((1 << (5 - LOGN)) - 1)) == 0 && t < nt) {
+        int hrow = hs[0];
+        float wt = ws[0];
+#pragma unroll
+        for (int tt = 1; tt < NT; ++tt)
+            if (tt == t) {
+                hrow = hs[tt];
+                wt = ws[tt];
+            }
+        acc_rows[rr * s.B + hrow / KS] += wt * dot;
+    }
+    return true;
+}
+
+template <int RW>
+__global__ void __launch_bounds__(DN3_THREADS, 2) down_v3_kernel(DownArgs a) {
+    constexpr int ES = RW;              // expert splits
+    constexpr int SW = DN3_CW / ES;     // warps per split
+    static_assert(SW * RW == DN3_RT, "8 rows per CTA");
+    extern __shared__ __align__(128) int smem_i[];
+    const DecodeShape s = a.s;
+    const RouteMap m = carve_map(smem_i, s, true);
+    float* acc = reinterpret_cast<float*>(smem_i + map_ints(s, true));  // [ES][DN3_RT][B]
+    const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_i) + dn3_smem_offset(s, RW);
+    char* ring = reinterpret_cast<char*>((raw + 127) & ~uintptr_t(127));
+    const DN3Layout L = dn3_layout(s, RW);
+    // slot (split h, k) = h * L.S + k
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)ES * L.S * L.stage_bytes);
+    uint64_t* empty = full + DN3_SMAX;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < ES * L.S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], SW);
+        }
+        mbar_init_fence();
+    }
+    build_route_map(m, a.ids, a.w, s, a.err, true);  // ends with __syncthreads
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int o0 = blockIdx.x * DN3_RT;
+    const int nu = m.hdr[0];
+    bool ok = true;
+
+    if (warp == DN3_CW) {
+        // ---------------- producer ----------------
+        const uint64_t pol = l2_evict_first_policy();
+        const int nb = s.I / 32;
+        const uint32_t wbytes = DN3_RT * s.I, sbytes = DN3_RT * nb;
+        // stage j -> split j % ES, its n = j / ES-th stage, slot n % S, use n / S
+        auto slot_of = [&](uint32_t j) { return (int)((j % ES) * L.S + (j / ES) % L.S); };
+        auto issue_w = [&](int u, int t0, uint32_t j) {
+            const int nt = min(TC, m.ucnt[u] - t0);
+            const int e = m.uexp[u];
+            const bool sh = e >= s.E;
+            const MXView vd = sh ? a.shd : a.wd;
+            const size_t r0 = (sh ? 0 : (size_t)e) * s.d + o0;
+            const int slot = slot_of(j);
+            char* st = ring + (size_t)slot * L.stage_bytes;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full[slot], wbytes + sbytes + nt * s.I * 2);
+                fence_proxy_async();
+                bulk_g2s(st + L.w_off, vd.w + r0 * s.I, wbytes, &full[slot], pol);
+                bulk_g2s(st + L.s_off, vd.s + r0 * nb, sbytes, &full[slot], pol);
+            }
+        };
+        auto issue_h = [&](int u, int t0, uint32_t j) {
+            const int nt = min(TC, m.ucnt[u] - t0);
+            const int slot = slot_of(j);
+            char* st = ring + (size_t)slot * L.stage_bytes;
+            if (lane < nt) {
+                fence_proxy_async();
+                bulk_g2s_keep(st + L.h_off + (size_t)lane * s.I * 2,
+                              a.h + (size_t)m.hrow[m.uoff[u] + t0 + lane] * s.I, s.I * 2, &full[slot]);
+            }
+        };
+        auto advance = [&](int& u, int& t0) {
+            t0 += TC;
+            if (t0 >= m.ucnt[u]) {
+                t0 = 0;
+                ++u;
+            }
+        };
+        // the first ES * S stages fill fresh slots; their weights do not
+        // depend on the gate/up pass
+        int pu = 0, pt = 0;
+        uint32_t j = 0;
+        for (; j < (uint32_t)(ES * L.S) && pu < nu; ++j) {
+            issue_w(pu, pt, j);
+            advance(pu, pt);
+        }
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        int hu = 0, ht = 0;
+        for (uint32_t i = 0; i < j; ++i) {
+            issue_h(hu, ht, i);
+            advance(hu, ht);
+        }
+        for (; pu < nu; ++j) {
+            const uint32_t n = j / ES;
+            if (!mbar_wait(&empty[slot_of(j)], ((n / L.S) - 1) & 1)) {
+                ok = false;
+                break;
+            }
+            issue_w(pu, pt, j);
+            __syncwarp();
+            issue_h(pu, pt, j);
+            advance(pu, pt);
+        }
+        // never leave the CTA with a copy in flight
+        for (uint32_t i = j > (uint32_t)(ES * L.S) ? j - ES * L.S : 0; i < j; ++i)
+            mbar_wait(&full[slot_of(i)], ((i / ES) / L.S) & 1);
+    } else {
+        // ---------------- consumers ----------------
+        const int split = warp / SW, cw = warp % SW;
+        float* acc_rows = acc + (size_t)(split * DN3_RT + cw * RW) * s.B;
+        for (int i = lane; i < RW * s.B; i += 32) acc_rows[i] = 0.f;
+        __syncwarp();
+        uint32_t j0 = 0;  // global index of u's first stage
+        for (int u = 0; u < nu && ok; ++u) {
+            const int cnt = m.ucnt[u], s0 = m.uoff[u];
+            const int groups = (cnt + TC - 1) / TC;
+            // u's stages are j0 .. j0 + groups - 1; this split takes j % ES == split
+            for (int g = (split - (int)(j0 % ES) + ES) % ES; g < groups && ok; g += ES) {
+                const int t0 = g * TC;
+                const int nt = min(TC, cnt - t0);
+                const uint32_t jj = j0 + g, n = jj / ES;
+                const int slot = split * L.S + (int)(n % L.S);
+                const char* st = ring + (size_t)slot * L.stage_bytes;
+                const uint32_t par = (n / L.S) & 1;
+                const int* hs = m.hrow + s0 + t0;
+                const float* wsp = m.wt + s0 + t0;
+                switch (nt) {
+                    case 1: ok = dn3_group<RW, 1>(a, L, st, &full[slot], &empty[slot], par, cw, lane, hs, wsp, nt, acc_rows); break;
+                    case 2: ok = dn3_group<RW, 2>(a, L, st, &full[slot], &empty[slot], par, cw, lane, hs, wsp, nt, acc_rows); break;
+                    case 3: ok = dn3_group<RW, 3>(a, L, st, &full[slot], &empty[slot], par, cw, lane, hs, wsp, nt, acc_rows); break;
+                    default: ok = dn3_group<RW, 4>(a, L, st, &full[slot], &empty[slot], par, cw, lane, hs, wsp, nt, acc_rows); break;
+                }
+            }
+            j0 += groups;
+        }
+    }
+    // add the expert splits in a fixed order and round once to BF16
+    __syncthreads();
+    for (int i = threadIdx.x; i < DN3_RT * s.B; i += blockDim.x) {
+        const int r = i / s.B, b = i - r * s.B;
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < ES; ++q) sum += acc[(size_t)q * DN3_RT * s.B + i];
+        a.y[(size_t)b * s.d + o0 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+    }
+    if (!ok && lane == 0) atomicOr(a.err, MOE_DEVERR_TIMEOUT);
+}
+
 // -------------------------------------------------------------- host -----
 
 // Lanes per weight row: the largest power of two <= 32 that divides the
@@ -478,6 +1455,137 @@ static cudaError_t launch_gate_up_L(const GateUpArgs& a, size_t smem, const Devi
     return cudaGetLastError();
 }
 
+#ifndef MOEDEC_GU2_FOLD
+#define MOEDEC_GU2_FOLD 0
+#endif
+
+static bool gate_up_v2_ok(const DecodeShape& s) { return s.d % 128 == 0; }
+
+static size_t gate_up_v2_smem(const DecodeShape& s) {
+    return map_ints(s, false) * 4 + (size_t)DEC_WARPS * sizeof(GU2Ring);
+}
+
+static cudaError_t launch_gate_up_v2(const GateUpArgs& a, const DeviceInfo& di, int dev, cudaStream_t st) {
+    const size_t smem = gate_up_v2_smem(a.s);
+    int bps = 1;
+    cudaError_t err = prepare(gate_up_v2_kernel<MOEDEC_GU2_FOLD != 0>, smem, dev, &bps);
+    if (err != cudaSuccess) return err;
+    const long items = (long)max_unique(a.s) * (a.s.I / 2);
+    long grid = std::min<long>((long)di.sm_count * bps, (items + DEC_WARPS - 1) / DEC_WARPS);
+    if (grid < 1) grid = 1;
+    gate_up_v2_kernel<MOEDEC_GU2_FOLD != 0><<<(unsigned)grid, DEC_THREADS, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Bulk copies need 16-byte aligned sources: weight and x rows are (d % 512),
+// the scale rows are too when the scale arrays themselves are.
+static bool gate_up_v3_ok(const GateUpArgs& a) {
+    const DecodeShape& s = a.s;
+    if (s.d % GU3_KT || s.I % GU3_ROWS) return false;
+    if (!aligned16(a.wg.s) || !aligned16(a.wu.s)) return false;
+    if (s.S && (!aligned16(a.shg.s) || !aligned16(a.shu.s))) return false;
+    return true;
+}
+
+static size_t gate_up_v3_smem(const DecodeShape& s) { return gu3_smem_offset(s) + sizeof(GU3Smem) + 128; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2D uint8 tensor map over [rows][cols] (row stride = cols bytes); cached by
+// (address, rows, cols, box) so repeated calls on the same weights do not
+// re-encode.
+static bool map_2d_u8(CUtensorMap* out, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                      uint32_t box_cols) {
+    static std::mutex mu;
+    static std::map<std::tuple<const void*, uint64_t, uint64_t, uint32_t, uint32_t>, CUtensorMap> cache;
+    const auto key = std::make_tuple(base, rows, cols, box_rows, box_cols);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+        *out = it->second;
+        return true;
+    }
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    CUtensorMap m;
+    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    if (cache.size() > 1024) cache.clear();
+    cache[key] = m;
+    *out = m;
+    return true;
+}
+
+static bool gate_up_v3_maps(const GateUpArgs& a, GU3Maps* maps) {
+    const DecodeShape& s = a.s;
+    const MXView v[2][2] = {{a.wg, a.wu}, {a.shg, a.shu}};
+    for (int sh = 0; sh < 2; ++sh) {
+        const uint64_t rows = (uint64_t)(sh ? 1 : s.E) * s.I;
+        for (int p = 0; p < 2; ++p) {
+            const MXView& m = sh && !s.S ? v[0][p] : v[sh][p];  // no shared expert: any valid map
+            const uint64_t r = sh && !s.S ? (uint64_t)s.E * s.I : rows;
+            if (!map_2d_u8(&maps->w[sh][p], m.w, r, s.d, GU3_ROWS, GU3_BOX)) return false;
+            if (!map_2d_u8(&maps->s[sh][p], m.s, r, s.d / 32, GU3_ROWS, 16)) return false;
+        }
+    }
+    return true;
+}
+
+static cudaError_t launch_gate_up_v3(const GateUpArgs& a, const GU3Maps& maps, const DeviceInfo& di, int dev,
+                                     cudaStream_t st) {
+    const size_t smem = gate_up_v3_smem(a.s);
+    static std::mutex mu;
+    static int bps_cache[64] = {0};
+    static size_t smem_cache[64] = {0};
+    int bps = 1;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && bps_cache[dev] && smem_cache[dev] >= smem) {
+            bps = bps_cache[dev];
+        } else {
+            cudaError_t err = cudaFuncSetAttribute(gate_up_v3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)std::max<size_t>(smem, 48 * 1024));
+            if (err != cudaSuccess) return err;
+            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, gate_up_v3_kernel, GU3_THREADS, smem);
+            if (err != cudaSuccess) return err;
+            if (bps < 1) bps = 1;
+            if (dev < 64) {
+                bps_cache[dev] = bps;
+                smem_cache[dev] = smem;
+            }
+        }
+    }
+    const long tiles = (long)max_unique(a.s) * (a.s.I / GU3_ROWS);
+    long grid = std::min<long>((long)di.sm_count * bps, tiles);
+    if (grid < 1) grid = 1;
+    gate_up_v3_kernel<<<(unsigned)grid, GU3_THREADS, smem, st>>>(a, maps);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gate_up(const DecodeShape& s, const void* x, const int32_t* ids, MXView wg,
                            MXView wu, MXView shg, MXView shu, void* h, cudaStream_t st) {
     DeviceInfo di;
@@ -486,6 +1594,14 @@ cudaError_t launch_gate_up(const DecodeShape& s, const void* x, const int32_t* i
     int dev = 0;
     cudaGetDevice(&dev);
     GateUpArgs a{s, (const uint16_t*)x, ids, wg, wu, shg, shu, (uint16_t*)h, di.err_word};
+#ifndef MOEDEC_NO_GU3
+    if (gate_up_v3_ok(a) && gate_up_v3_smem(s) <= (size_t)di.max_smem_optin) {
+        GU3Maps maps;
+        if (gate_up_v3_maps(a, &maps)) return launch_gate_up_v3(a, maps, di, dev, st);
+    }
+#endif
+    if (gate_up_v2_ok(s) && gate_up_v2_smem(s) <= (size_t)di.max_smem_optin)
+        return launch_gate_up_v2(a, di, dev, st);
     const size_t smem = gate_up_smem_bytes(s);
     switch (lanes_per_row(s.d)) {
         case 32: return launch_gate_up_L<32>(a, smem, di, dev, st);
@@ -531,6 +1647,98 @@ static cudaError_t launch_down_L(DownArgs a, size_t smem, const DeviceInfo& di, 
     return cudaLaunchKernelEx(&cfg, down_kernel<L>, a);
 }
 
+static int down_v2_lanes(const DecodeShape& s) {
+    if (s.I % 512 == 0) return 32;
+    if (s.I % 256 == 0) return 16;
+    if (s.I % 128 == 0) return 8;
+    return 0;
+}
+
+static size_t down_v2_smem(const DecodeShape& s, int L) {
+    const int G = 32 / L;
+    const size_t acc_n = (size_t)DEC_WARPS * G * DN2_R * s.B;
+    return map_ints(s, true) * 4 + (acc_n + 3) / 4 * 4 * 4 + (size_t)DEC_WARPS * sizeof(DN2Ring);
+}
+
+template <int L>
+static cudaError_t launch_down_v2_L(DownArgs a, size_t smem, const DeviceInfo& di, int dev,
+                                    cudaStream_t st, bool pdl) {
+    int bps = 1;
+    cudaError_t err = prepare(down_v2_kernel<L>, smem, dev, &bps);
+    if (err != cudaSuccess) return err;
+    constexpr int G = 32 / L;
+    const long target_warps = (long)di.sm_count * 16;
+    const int mu = max_unique(a.s);
+    int es = 1;
+    while (es < DEC_WARPS && es * 2 <= mu) {
+        const long rt = (long)(DEC_WARPS / es) * G * DN2_R;
+        const long warps = (a.s.d + rt - 1) / rt * DEC_WARPS;
+        if (warps >= target_warps) break;
+        es *= 2;
+    }
+    a.es = es;
+    const int RT = (DEC_WARPS / es) * G * DN2_R;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((a.s.d + RT - 1) / RT));
+    cfg.blockDim = dim3(DEC_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, down_v2_kernel<L>, a);
+}
+
+// Bulk copies: the [8 rows x I] weight block and its scale block must start
+// on 16-byte boundaries (I % 256 == 0 keeps them there when the arrays do).
+static bool down_v3_ok(const DecodeShape& s, MXView wd, MXView shd) {
+    if (s.I % 256 || s.d % DN3_RT) return false;
+    if (!aligned16(wd.s) || (s.S && !aligned16(shd.s))) return false;
+    return true;
+}
+
+static size_t down_v3_smem(const DecodeShape& s) {
+    const int RW = dn3_rw(s.I);
+    const DN3Layout L = dn3_layout(s, RW);
+    if (L.S < 2) return ~(size_t)0;  // ring too small for this shape
+    return dn3_smem_offset(s, RW) + (size_t)RW * L.S * L.stage_bytes + 2 * DN3_SMAX * sizeof(uint64_t) + 128;
+}
+
+template <int RW>
+static cudaError_t launch_down_v3_rw(const DownArgs& a, size_t smem, int dev, cudaStream_t st, bool pdl) {
+    static std::mutex mu;
+    static size_t attr_smem[64] = {0};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= 64 || attr_smem[dev] < smem) {
+            cudaError_t err = cudaFuncSetAttribute(down_v3_kernel<RW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)std::max<size_t>(smem, 48 * 1024));
+            if (err != cudaSuccess) return err;
+            if (dev < 64) attr_smem[dev] = smem;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.s.d / DN3_RT));
+    cfg.blockDim = dim3(DN3_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, down_v3_kernel<RW>, a);
+}
+
+static cudaError_t launch_down_v3(const DownArgs& a, size_t smem, int dev, cudaStream_t st, bool pdl) {
+    switch (dn3_rw(a.s.I)) {
+        case 1: return launch_down_v3_rw<1>(a, smem, dev, st, pdl);
+        default: return launch_down_v3_rw<2>(a, smem, dev, st, pdl);
+    }
+}
+
 cudaError_t launch_down(const DecodeShape& s, const void* h, const int32_t* ids, const float* w,
                         MXView wd, MXView shd, void* y, cudaStream_t st, bool after_gate_up) {
     DeviceInfo di;
@@ -539,6 +1747,23 @@ cudaError_t launch_down(const DecodeShape& s, const void* h, const int32_t* ids,
     int dev = 0;
     cudaGetDevice(&dev);
     DownArgs a{s, (const uint16_t*)h, ids, w, wd, shd, (uint16_t*)y, di.err_word, 1};
+#ifndef MOEDEC_NO_DN3
+    if (down_v3_ok(s, wd, shd)) {
+        const size_t smem3 = down_v3_smem(s);
+        if (smem3 <= (size_t)di.max_smem_optin) return launch_down_v3(a, smem3, dev, st, after_gate_up);
+    }
+#endif
+    const int L2 = down_v2_lanes(s);
+    if (L2) {
+        const size_t smem2 = down_v2_smem(s, L2);
+        if (smem2 <= (size_t)di.max_smem_optin) {
+            switch (L2) {
+                case 32: return launch_down_v2_L<32>(a, smem2, di, dev, st, after_gate_up);
+                case 16: return launch_down_v2_L<16>(a, smem2, di, dev, st, after_gate_up);
+                default: return launch_down_v2_L<8>(a, smem2, di, dev, st, after_gate_up);
+            }
+        }
+    }
     const size_t smem = down_smem_bytes(s);
     switch (lanes_per_row(s.I)) {
         case 32: return launch_down_L<32>(a, smem, di, dev, st, after_gate_up);
