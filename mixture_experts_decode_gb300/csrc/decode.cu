@@ -66,6 +66,7 @@ struct RouteMap {
     int* sid;   // [B * k] expert id of each slot (-1 if out of range)
     int* wtot;  // [DEC_WARPS] scan scratch
     int* ucnt;  // [max_unique] slots per distinct expert after merging duplicates (down)
+    int* tok;   // [slots] token of each entry (down)
 };
 
 __host__ __device__ inline int max_unique(const DecodeShape& s) {
@@ -76,7 +77,7 @@ __host__ __device__ inline int n_slots(const DecodeShape& s) { return s.B * s.k 
 
 __host__ __device__ inline size_t map_ints(const DecodeShape& s, bool with_w) {
     const size_t mu = (size_t)max_unique(s);
-    size_t ints = 4 + mu + (mu + 1) + n_slots(s) + (with_w ? n_slots(s) + mu : 0) + s.E +
+    size_t ints = 4 + mu + (mu + 1) + n_slots(s) + (with_w ? 2 * n_slots(s) + mu : 0) + s.E +
                   (size_t)s.B * s.k + DEC_WARPS;
     return (ints + 3) / 4 * 4;  // keep what follows 16-byte aligned
 }
@@ -105,6 +106,8 @@ __device__ RouteMap carve_map(int* p, const DecodeShape& s, bool with_w) {
     m.wtot = p;
     p += DEC_WARPS;
     m.ucnt = with_w ? p : nullptr;
+    if (with_w) p += mu;
+    m.tok = with_w ? p : nullptr;
     return m;
 }
 
@@ -230,11 +233,13 @@ __device__ void build_route_map(const RouteMap& m, const int32_t* __restrict__ i
                 int wpos = i0;
                 for (int i = i0; i < i1; ++i) {
                     const int hr = m.hrow[i];
-                    if (wpos > i0 && hr / KS == m.hrow[wpos - 1] / KS) {
+                    const int b = hr / KS;
+                    if (wpos > i0 && b == m.tok[wpos - 1]) {
                         m.wt[wpos - 1] += m.wt[i];
                     } else {
                         m.hrow[wpos] = hr;
                         m.wt[wpos] = m.wt[i];
+                        m.tok[wpos] = b;
                         ++wpos;
                     }
                 }
@@ -1164,7 +1169,13 @@ constexpr int DN3_CW = 8;                       // consumer warps
 constexpr int DN3_THREADS = (DN3_CW + 1) * 32;  // + producer warp
 constexpr int DN3_RT = 8;                       // rows per CTA
 constexpr int DN3_SMAX = 8;                     // ring slots (all splits)
-constexpr int DN3_RING_BYTES = 80 * 1024;  // two CTAs per SM
+#ifndef MOEDEC_DN3_RING
+#define MOEDEC_DN3_RING (80 * 1024)
+#endif
+#ifndef MOEDEC_DN3_MINS
+#define MOEDEC_DN3_MINS 1
+#endif
+constexpr int DN3_RING_BYTES = MOEDEC_DN3_RING;  // two CTAs per SM
 
 struct DN3Layout {
     int stage_bytes, w_off, s_off, h_off, S;  // S = slots per split
@@ -1189,18 +1200,20 @@ __host__ __device__ inline size_t dn3_smem_offset(const DecodeShape& s, int RW) 
 
 // Rows per warp (= expert splits) for a given I: at least ~48 weight bytes
 // per lane per stage, and at least two ring slots per split.
-__host__ __device__ inline int dn3_rw(int I) { return I >= 2048 ? 1 : 2; }
+#ifndef MOEDEC_DN3_RWSMALL
+#define MOEDEC_DN3_RWSMALL 4
+#endif
+__host__ __device__ inline int dn3_rw(int I) { return I >= 2048 ? 1 : MOEDEC_DN3_RWSMALL; }
 
 template <int RW, int NT>
 __device__ __forceinline__ bool dn3_group(const DownArgs& a, const DN3Layout& L, const char* st, uint64_t* full,
-                                          uint64_t* empty, uint32_t parity, int cw, int lane, const int* hs,
+                                          uint64_t* empty, uint32_t parity, int cw, int lane, const int* toks,
                                           const float* ws, int nt, float* acc_rows) {
     constexpr int NTP = NT == 3 ? 4 : NT;
     const DecodeShape& s = a.s;
-    const int KS = s.k + s.S;
     if (!mbar_wait(full, parity)) return false;
-    const uint8_t* wb = reinterpret_cast<const uint8_t*>(st + L.w_off);
-    const uint8_t* sb = reinterpret_cast<const uint8_t*>(st + L.s_off);
+    const uint8_t* wb = reinterpret_cast<const uint8_t*>(st + L.w_off) + (size_t)cw * RW * s.I;
+    const uint8_t* sb = reinterpret_cast<const uint8_t*>(st + L.s_off) + cw * RW * (s.I / 32);
     const uint16_t* hb = reinterpret_cast<const uint16_t*>(st + L.h_off);
     float2 acc[RW][NT];
 #pragma unroll
@@ -1210,23 +1223,26 @@ __device__ __forceinline__ bool dn3_group(const DownArgs& a, const DN3Layout& L,
     const int nch = s.I / 256;  // 8-byte chunks per lane
     for (int i = 0; i < nch; ++i) {
         const int k0 = (lane + 32 * i) * 8;  // first K element of this chunk
-        uint4 hv[NT];
+        float2 hf[NT][4];  // the tokens' eight activations, converted once for all rows
 #pragma unroll
-        for (int t = 0; t < NT; ++t) hv[t] = *reinterpret_cast<const uint4*>(hb + (size_t)t * s.I + k0);
+        for (int t = 0; t < NT; ++t) {
+            const uint4 hv = *reinterpret_cast<const uint4*>(hb + (size_t)t * s.I + k0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) hf[t][q] = bf16x2_to_float2((&hv.x)[q]);
+        }
 #pragma unroll
         for (int r = 0; r < RW; ++r) {
-            const int row = cw * RW + r;
-            const uint2 wv = *reinterpret_cast<const uint2*>(wb + (size_t)row * s.I + k0);
-            const float sc = e8m0_to_float(sb[row * (s.I / 32) + (k0 >> 5)]);
+            const uint2 wv = *reinterpret_cast<const uint2*>(wb + (size_t)r * s.I + k0);
+            const float sc = e8m0_to_float(sb[r * (s.I / 32) + (k0 >> 5)]);
             float2 wq[4];
             e4m3x4_to_float(wv.x, wq[0], wq[1]);
             e4m3x4_to_float(wv.y, wq[2], wq[3]);
             // the chunk lies inside one scale block: scale its partial sum once
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
-                float2 part = __fmul2_rn(bf16x2_to_float2(hv[t].x), wq[0]);
+                float2 part = __fmul2_rn(hf[t][0], wq[0]);
 #pragma unroll
-                for (int q = 1; q < 4; ++q) part = __ffma2_rn(bf16x2_to_float2((&hv[t].x)[q]), wq[q], part);
+                for (int q = 1; q < 4; ++q) part = __ffma2_rn(hf[t][q], wq[q], part);
                 acc[r][t] = __ffma2_rn(part, make_float2(sc, sc), acc[r][t]);
             }
         }
@@ -1246,15 +1262,15 @@ __device__ __forceinline__ bool dn3_group(const DownArgs& a, const DN3Layout& L,
     const int idx = (lane >> (5 - LOGN)) & (N - 1);
     const int rr = idx / NTP, t = idx % NTP;
     if ((lane & ((1 << (5 - LOGN)) - 1)) == 0 && t < nt) {
-        int hrow = hs[0];
+        int b = toks[0];
         float wt = ws[0];
 #pragma unroll
         for (int tt = 1; tt < NT; ++tt)
             if (tt == t) {
-                hrow = hs[tt];
+                b = toks[tt];
                 wt = ws[tt];
             }
-        acc_rows[rr * s.B + hrow / KS] += wt * dot;
+        acc_rows[rr * s.B + b] += wt * dot;
     }
     return true;
 }
@@ -1362,6 +1378,8 @@ __global__ void __launch_bounds__(DN3_THREADS, 2) down_v3_kernel(DownArgs a) {
         for (int i = lane; i < RW * s.B; i += 32) acc_rows[i] = 0.f;
         __syncwarp();
         uint32_t j0 = 0;  // global index of u's first stage
+        int k = 0;        // ring slot of this split's next stage
+        uint32_t par = 0; // its phase parity
         for (int u = 0; u < nu && ok; ++u) {
             const int cnt = m.ucnt[u], s0 = m.uoff[u];
             const int groups = (cnt + TC - 1) / TC;
@@ -1369,17 +1387,19 @@ __global__ void __launch_bounds__(DN3_THREADS, 2) down_v3_kernel(DownArgs a) {
             for (int g = (split - (int)(j0 % ES) + ES) % ES; g < groups && ok; g += ES) {
                 const int t0 = g * TC;
                 const int nt = min(TC, cnt - t0);
-                const uint32_t jj = j0 + g, n = jj / ES;
-                const int slot = split * L.S + (int)(n % L.S);
+                const int slot = split * L.S + k;
                 const char* st = ring + (size_t)slot * L.stage_bytes;
-                const uint32_t par = (n / L.S) & 1;
-                const int* hs = m.hrow + s0 + t0;
+                const int* tk = m.tok + s0 + t0;
                 const float* wsp = m.wt + s0 + t0;
                 switch (nt) {
-                    case 1: ok = dn3_group<RW, 1>(a, L, st, &full[slot], &empty[slot], par, cw, lane, hs, wsp, nt, acc_rows); break;
-                    case 2: ok = dn3_group<RW, 2>(a, L, st, &full[slot], &empty[slot], par, cw, lane, hs, wsp, nt, acc_rows); break;
-                    case 3: ok = dn3_group<RW, 3>(a, L, st, &full[slot], &empty[slot], par, cw, lane, hs, wsp, nt, acc_rows); break;
-                    default: ok = dn3_group<RW, 4>(a, L, st, &full[slot], &empty[slot], par, cw, lane, hs, wsp, nt, acc_rows); break;
+                    case 1: ok = dn3_group<RW, 1>(a, L, st, &full[slot], &empty[slot], par, cw, lane, tk, wsp, nt, acc_rows); break;
+                    case 2: ok = dn3_group<RW, 2>(a, L, st, &full[slot], &empty[slot], par, cw, lane, tk, wsp, nt, acc_rows); break;
+                    case 3: ok = dn3_group<RW, 3>(a, L, st, &full[slot], &empty[slot], par, cw, lane, tk, wsp, nt, acc_rows); break;
+                    default: ok = dn3_group<RW, 4>(a, L, st, &full[slot], &empty[slot], par, cw, lane, tk, wsp, nt, acc_rows); break;
+                }
+                if (++k == L.S) {
+                    k = 0;
+                    par ^= 1;
                 }
             }
             j0 += groups;
@@ -1702,7 +1722,7 @@ static bool down_v3_ok(const DecodeShape& s, MXView wd, MXView shd) {
 static size_t down_v3_smem(const DecodeShape& s) {
     const int RW = dn3_rw(s.I);
     const DN3Layout L = dn3_layout(s, RW);
-    if (L.S < 2) return ~(size_t)0;  // ring too small for this shape
+    if (L.S < MOEDEC_DN3_MINS) return ~(size_t)0;  // ring too small for this shape
     return dn3_smem_offset(s, RW) + (size_t)RW * L.S * L.stage_bytes + 2 * DN3_SMAX * sizeof(uint64_t) + 128;
 }
 
@@ -1735,7 +1755,11 @@ static cudaError_t launch_down_v3_rw(const DownArgs& a, size_t smem, int dev, cu
 static cudaError_t launch_down_v3(const DownArgs& a, size_t smem, int dev, cudaStream_t st, bool pdl) {
     switch (dn3_rw(a.s.I)) {
         case 1: return launch_down_v3_rw<1>(a, smem, dev, st, pdl);
+#if MOEDEC_DN3_RWSMALL == 4
+        default: return launch_down_v3_rw<4>(a, smem, dev, st, pdl);
+#else
         default: return launch_down_v3_rw<2>(a, smem, dev, st, pdl);
+#endif
     }
 }
 
