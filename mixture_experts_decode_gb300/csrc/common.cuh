@@ -183,20 +183,22 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Wait for the phase with the given parity to complete.  Bounded: gives up
-// after ~2^32 SM cycles (about two seconds), returning false.
+// Wait for the phase with the given parity to complete.  Each try_wait
+// suspends the thread (until the phase completes or a ~0.5 ms hint runs
+// out) instead of spinning, so waiting warps take no issue slots.  Bounded:
+// gives up after ~2^32 SM cycles (about two seconds), returning false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     const uint32_t a = smem_addr(bar);
     uint32_t ok = 0;
-    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-                 : "=r"(ok) : "r"(a), "r"(parity) : "memory");
-    if (ok) return true;
     const long long t0 = clock64();
-    while (clock64() - t0 < (1ll << 32)) {
-        asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-                     : "=r"(ok) : "r"(a), "r"(parity) : "memory");
+    do {
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+            : "=r"(ok)
+            : "r"(a), "r"(parity), "r"(500000u)
+            : "memory");
         if (ok) return true;
-    }
+    } while (clock64() - t0 < (1ll << 32));
     return false;
 }
 

@@ -1417,6 +1417,197 @@ __global__ void __launch_bounds__(DN3_THREADS, 2) down_v3_kernel(DownArgs a) {
     if (!ok && lane == 0) atomicOr(a.err, MOE_DEVERR_TIMEOUT);
 }
 
+// ------------------------------------------------------------ down v4 ----
+// Like down v3, but every consumer warp takes every stage, in order (one
+// ring, so no barrier phase is ever skipped), each warp owning RW rows of a
+// block of RT = 8 * RW output rows; and a thread-block cluster of CL CTAs
+// shares one row block, CTA rank r taking the distinct experts u with
+// u % CL == r.  At the end the CL partial accumulators are added through
+// distributed shared memory, in rank order, each CTA rounding and storing
+// RT / CL of the rows.  Larger blocks mean bigger bulk copies and fewer h
+// reads; the cluster split keeps enough CTAs.
+
+constexpr int DN4_CW = 8;
+constexpr int DN4_THREADS = (DN4_CW + 1) * 32;
+constexpr int DN4_SMAX = 8;
+constexpr int DN4_RING_BYTES = 96 * 1024;  // two CTAs per SM
+
+__host__ __device__ inline DN3Layout dn4_layout(const DecodeShape& s, int RW) {
+    const int RT = DN4_CW * RW;
+    DN3Layout L;
+    L.w_off = 0;
+    L.s_off = RT * s.I;
+    L.h_off = (L.s_off + RT * (s.I / 32) + 127) / 128 * 128;
+    L.stage_bytes = (L.h_off + TC * s.I * 2 + 127) / 128 * 128;
+    const int S = DN4_RING_BYTES / L.stage_bytes;
+    L.S = S > DN4_SMAX ? DN4_SMAX : S;
+    return L;
+}
+
+__host__ __device__ inline size_t dn4_smem_offset(const DecodeShape& s, int RW) {
+    const size_t acc = (size_t)DN4_CW * RW * s.B * 4;
+    return (map_ints(s, true) * 4 + acc + 127) / 128 * 128;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+    return v;
+}
+
+template <int RW, int CL>
+__global__ void __launch_bounds__(DN4_THREADS, 2) down_v4_kernel(DownArgs a) {
+    constexpr int RT = DN4_CW * RW;
+    extern __shared__ __align__(128) int smem_i[];
+    const DecodeShape s = a.s;
+    const RouteMap m = carve_map(smem_i, s, true);
+    float* acc = reinterpret_cast<float*>(smem_i + map_ints(s, true));  // [RT][B]
+    const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_i) + dn4_smem_offset(s, RW);
+    char* ring = reinterpret_cast<char*>((raw + 127) & ~uintptr_t(127));
+    const DN3Layout L = dn4_layout(s, RW);
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)L.S * L.stage_bytes);
+    uint64_t* empty = full + DN4_SMAX;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < L.S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], DN4_CW);
+        }
+        mbar_init_fence();
+    }
+    build_route_map(m, a.ids, a.w, s, a.err, true);  // ends with __syncthreads
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = CL > 1 ? (int)cluster_rank() : 0;
+    const int o0 = (blockIdx.x / CL) * RT;
+    const int nu = m.hdr[0];
+    bool ok = true;
+
+    if (warp == DN4_CW) {
+        // ---------------- producer ----------------
+        const uint64_t pol = l2_evict_first_policy();
+        const int nb = s.I / 32;
+        const uint32_t wbytes = RT * s.I, sbytes = RT * nb;
+        auto issue_w = [&](int u, int t0, int slot) {
+            const int nt = min(TC, m.ucnt[u] - t0);
+            const int e = m.uexp[u];
+            const bool sh = e >= s.E;
+            const MXView vd = sh ? a.shd : a.wd;
+            const size_t r0 = (sh ? 0 : (size_t)e) * s.d + o0;
+            char* st = ring + (size_t)slot * L.stage_bytes;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full[slot], wbytes + sbytes + nt * s.I * 2);
+                fence_proxy_async();
+                bulk_g2s(st + L.w_off, vd.w + r0 * s.I, wbytes, &full[slot], pol);
+                bulk_g2s(st + L.s_off, vd.s + r0 * nb, sbytes, &full[slot], pol);
+            }
+        };
+        auto issue_h = [&](int u, int t0, int slot) {
+            const int nt = min(TC, m.ucnt[u] - t0);
+            char* st = ring + (size_t)slot * L.stage_bytes;
+            if (lane < nt) {
+                fence_proxy_async();
+                bulk_g2s_keep(st + L.h_off + (size_t)lane * s.I * 2,
+                              a.h + (size_t)m.hrow[m.uoff[u] + t0 + lane] * s.I, s.I * 2, &full[slot]);
+            }
+        };
+        // this CTA's stages: experts u = rank, rank + CL, ..., each in groups of TC tokens
+        auto advance = [&](int& u, int& t0) {
+            t0 += TC;
+            if (t0 >= m.ucnt[u]) {
+                t0 = 0;
+                u += CL;
+            }
+        };
+        int pu = rank, pt = 0, npro = 0;
+        for (; npro < L.S && pu < nu; ++npro) {
+            issue_w(pu, pt, npro);
+            advance(pu, pt);
+        }
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        {
+            int hu = rank, ht = 0;
+            for (int i = 0; i < npro; ++i) {
+                issue_h(hu, ht, i);
+                advance(hu, ht);
+            }
+        }
+        uint32_t j = npro;
+        int slot = npro % L.S;
+        uint32_t par = 0;  // parity of the empty phase to wait for at `slot`
+        if (npro == L.S) slot = 0;
+        while (pu < nu) {
+            if (!mbar_wait(&empty[slot], par)) {
+                ok = false;
+                break;
+            }
+            issue_w(pu, pt, slot);
+            __syncwarp();
+            issue_h(pu, pt, slot);
+            advance(pu, pt);
+            ++j;
+            if (++slot == L.S) {
+                slot = 0;
+                par ^= 1;
+            }
+        }
+        for (uint32_t i = j > (uint32_t)L.S ? j - L.S : 0; i < j; ++i) mbar_wait(&full[i % L.S], (i / L.S) & 1);
+    } else {
+        // ---------------- consumers ----------------
+        float* acc_rows = acc + (size_t)(warp * RW) * s.B;
+        for (int i = lane; i < RW * s.B; i += 32) acc_rows[i] = 0.f;
+        __syncwarp();
+        int slot = 0;
+        uint32_t par = 0;
+        for (int u = rank; u < nu && ok; u += CL) {
+            const int cnt = m.ucnt[u], s0 = m.uoff[u];
+            for (int t0 = 0; t0 < cnt && ok; t0 += TC) {
+                const int nt = min(TC, cnt - t0);
+                const char* st = ring + (size_t)slot * L.stage_bytes;
+                const int* tk = m.tok + s0 + t0;
+                const float* wsp = m.wt + s0 + t0;
+                switch (nt) {
+                    case 1: ok = dn3_group<RW, 1>(a, L, st, &full[slot], &empty[slot], par, warp, lane, tk, wsp, nt, acc_rows); break;
+                    case 2: ok = dn3_group<RW, 2>(a, L, st, &full[slot], &empty[slot], par, warp, lane, tk, wsp, nt, acc_rows); break;
+                    case 3: ok = dn3_group<RW, 3>(a, L, st, &full[slot], &empty[slot], par, warp, lane, tk, wsp, nt, acc_rows); break;
+                    default: ok = dn3_group<RW, 4>(a, L, st, &full[slot], &empty[slot], par, warp, lane, tk, wsp, nt, acc_rows); break;
+                }
+                if (++slot == L.S) {
+                    slot = 0;
+                    par ^= 1;
+                }
+            }
+        }
+    }
+    // add the cluster's partial sums in rank order; CTA `rank` stores rows
+    // [rank * RT / CL, (rank + 1) * RT / CL) of the block
+    __syncthreads();
+    if (CL > 1) cluster_sync_all();
+    constexpr int RR = RT / CL;
+    for (int i = threadIdx.x; i < RR * s.B; i += blockDim.x) {
+        const int rl = rank * RR + i / s.B, b = i % s.B;
+        const float* p = acc + (size_t)rl * s.B + b;
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < CL; ++q) sum += CL > 1 ? ld_cluster_f32(p, q) : *p;
+        a.y[(size_t)b * s.d + o0 + rl] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+    }
+    if (CL > 1) cluster_sync_all();  // keep this CTA's accumulators alive for its peers
+    if (!ok && lane == 0) atomicOr(a.err, MOE_DEVERR_TIMEOUT);
+}
+
 // -------------------------------------------------------------- host -----
 
 // Lanes per weight row: the largest power of two <= 32 that divides the
@@ -1763,6 +1954,76 @@ static cudaError_t launch_down_v3(const DownArgs& a, size_t smem, int dev, cudaS
     }
 }
 
+// Rows per warp for down v4: ~96 weight bytes per lane per stage.
+#ifndef MOEDEC_DN4_RWSMALL
+#define MOEDEC_DN4_RWSMALL 2
+#endif
+static int dn4_rw(int I) { return I >= 2048 ? 1 : (I >= 1024 ? 2 : MOEDEC_DN4_RWSMALL); }
+
+static size_t down_v4_smem(const DecodeShape& s, int RW) {
+    const DN3Layout L = dn4_layout(s, RW);
+    if (L.S < 2) return ~(size_t)0;
+    return dn4_smem_offset(s, RW) + (size_t)L.S * L.stage_bytes + 2 * DN4_SMAX * sizeof(uint64_t) + 128;
+}
+
+template <int RW, int CL>
+static cudaError_t launch_down_v4_k(const DownArgs& a, size_t smem, int dev, cudaStream_t st, bool pdl) {
+    static std::mutex mu;
+    static size_t attr_smem[64] = {0};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= 64 || attr_smem[dev] < smem) {
+            cudaError_t err = cudaFuncSetAttribute(down_v4_kernel<RW, CL>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)std::max<size_t>(smem, 48 * 1024));
+            if (err != cudaSuccess) return err;
+            if (dev < 64) attr_smem[dev] = smem;
+        }
+    }
+    constexpr int RT = DN4_CW * RW;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.s.d / RT * CL));
+    cfg.blockDim = dim3(DN4_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (CL > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = CL;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, down_v4_kernel<RW, CL>, a);
+}
+
+// Cluster size: enough CTAs to fill the GPU twice, never more than the
+// distinct experts a call can have.
+static int dn4_cl(const DecodeShape& s, int RW, int sm_count) {
+    const int blocks = s.d / (DN4_CW * RW);
+    int cl = 1;
+    while (cl < 4 && blocks * cl < 2 * sm_count * 3 / 4 && cl * 2 <= max_unique(s)) cl *= 2;
+    return cl;
+}
+
+template <int RW>
+static cudaError_t launch_down_v4_rw(const DownArgs& a, size_t smem, int dev, int sm_count, cudaStream_t st,
+                                     bool pdl) {
+    switch (dn4_cl(a.s, RW, sm_count)) {
+        case 1: return launch_down_v4_k<RW, 1>(a, smem, dev, st, pdl);
+        case 2: return launch_down_v4_k<RW, 2>(a, smem, dev, st, pdl);
+        default: return launch_down_v4_k<RW, 4>(a, smem, dev, st, pdl);
+    }
+}
+
 cudaError_t launch_down(const DecodeShape& s, const void* h, const int32_t* ids, const float* w,
                         MXView wd, MXView shd, void* y, cudaStream_t st, bool after_gate_up) {
     DeviceInfo di;
@@ -1771,6 +2032,21 @@ cudaError_t launch_down(const DecodeShape& s, const void* h, const int32_t* ids,
     int dev = 0;
     cudaGetDevice(&dev);
     DownArgs a{s, (const uint16_t*)h, ids, w, wd, shd, (uint16_t*)y, di.err_word, 1};
+#ifndef MOEDEC_NO_DN4
+    if (down_v3_ok(s, wd, shd)) {
+        const int RW = dn4_rw(s.I);
+        if (s.d % (DN4_CW * RW) == 0) {
+            const size_t smem4 = down_v4_smem(s, RW);
+            if (smem4 <= (size_t)di.max_smem_optin) {
+                switch (RW) {
+                    case 1: return launch_down_v4_rw<1>(a, smem4, dev, di.sm_count, st, after_gate_up);
+                    case 2: return launch_down_v4_rw<2>(a, smem4, dev, di.sm_count, st, after_gate_up);
+                    default: return launch_down_v4_rw<4>(a, smem4, dev, di.sm_count, st, after_gate_up);
+                }
+            }
+        }
+    }
+#endif
 #ifndef MOEDEC_NO_DN3
     if (down_v3_ok(s, wd, shd)) {
         const size_t smem3 = down_v3_smem(s);
