@@ -939,6 +939,297 @@ __global__ void __launch_bounds__(GU3_THREADS, MOEDEC_GU3_MINB)
     if (!ok && lane == 0) atomicOr(a.err, MOE_DEVERR_TIMEOUT);
 }
 
+// --------------------------------------------------------- gate/up v4 ----
+// Lane per weight row.  A tile = (distinct expert, RT rows of I); LPR = 32 /
+// RT lanes of every consumer warp own row n0 + r of both W_gate and W_up,
+// each lane a different 32-element scale block of it, so a lane sums whole
+// scale blocks by itself and scales each block's partial sum once.  The CW
+// consumer warps split every 512-element K stage into its 16 scale blocks,
+// warp w taking blocks w * LPR .. w * LPR + LPR - 1: per stage the warp
+// converts those blocks of each token's x to FP32 once, into its own small
+// buffer, and its lanes read them back as broadcasts.  The producer warp
+// brings each stage's RT x 512 code bytes of both projections as RT-row x
+// 128-byte tensor boxes stored in the 128-byte swizzled layout (chunk j of
+// row r lands at chunk j ^ (r & 7)), so lanes reading the same chunk of
+// consecutive rows hit distinct banks; plus the scale bytes and the tokens'
+// x slices.  After a tile's last stage the lanes of a row add their halves
+// by a shuffle, the warps' partial dots go through shared memory (double
+// buffered by token-group parity, one barrier per group) and 2 x RT x nt
+// threads, a pair per (token, row), add the CW warps in a fixed order,
+// apply SiLU(g) * u and store h.  Every wait is bounded; a wait that runs
+// out raises a CTA-wide abort flag so that all warps still pass every
+// barrier.  Two geometries: RT = 32 with 16 consumer warps and one CTA per
+// SM, RT = 16 with 8 consumer warps and two CTAs per SM.
+
+constexpr int GU4_KT = 512;   // K elements per stage (16 scale blocks)
+constexpr int GU4_BOX = 128;  // inner box of a weight tensor copy (bytes)
+constexpr int GU4_S = 4;      // ring stages
+
+template <int RT>
+struct __align__(1024) GU4Stage {
+    uint8_t w[2][GU4_KT / GU4_BOX][RT][GU4_BOX];  // [proj][box][row][128 B, swizzled]
+    uint8_t sc[2][RT][GU4_KT / 32];               // [proj][row][block] E8M0
+    uint16_t x[TC][GU4_KT];                       // BF16 activations of the slice
+};
+
+template <int RT, int CW>
+struct GU4Shared {
+    float xf[CW][TC][GU4_KT / CW];        // per warp: its blocks of x, FP32
+    float part[2][CW][2][TC][RT];         // [group parity][warp][proj][token][row] partial dots
+    uint64_t full[GU4_S];
+    uint64_t empty[GU4_S];
+    int abort;
+};
+
+struct GU4Maps {
+    CUtensorMap w[2][2];  // [routed / shared][gate / up], box RT rows x 128 B, 128-byte swizzle
+    CUtensorMap s[2][2];  // the same for the scales, box RT rows x 16 B
+};
+
+// Bounded wait that also gives up as soon as another warp raised `abort`;
+// a wait that runs out (~2^32 cycles) raises it.
+__device__ __forceinline__ bool mbar_wait_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    const uint32_t a = smem_addr(bar);
+    const long long t0 = clock64();
+    for (;;) {
+        uint32_t ok;
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+            : "=r"(ok)
+            : "r"(a), "r"(parity), "r"(20000u)
+            : "memory");
+        if (ok) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > (1ll << 32)) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+template <int NTHREADS>
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(NTHREADS) : "memory");
+}
+
+// Ring position of a thread: slot and the parity of the phase it waits for.
+struct RingPos {
+    int slot;
+    uint32_t par;
+    __device__ __forceinline__ void next(int S) {
+        if (++slot == S) {
+            slot = 0;
+            par ^= 1u;
+        }
+    }
+};
+
+__host__ __device__ inline size_t gu4_ring_offset(const DecodeShape& s) { return map_ints(s, false) * 4; }
+
+template <int RT, int CW, int NT>
+__device__ __forceinline__ void gu4_group(const GateUpArgs& a, GU4Stage<RT>* ring, GU4Shared<RT, CW>* sh,
+                                          RingPos& rp, int grp, int nkt, int warp, int lane, int n0,
+                                          const int* hs) {
+    constexpr int LPR = 32 / RT;       // lanes per row
+    constexpr int KW = GU4_KT / CW;    // K elements of a warp per stage (= 32 * LPR)
+    static_assert(KW == 32 * LPR, "one scale block per lane");
+    const DecodeShape& s = a.s;
+    float2 acc[2][NT];
+#pragma unroll
+    for (int p = 0; p < 2; ++p)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[p][t] = make_float2(0.f, 0.f);
+    const int r = lane % RT, hb = lane / RT;   // row, which of the warp's blocks
+    const int blk = warp * LPR + hb;           // scale block within the stage
+    const int box = blk >> 2, c0 = (blk & 3) * 2, sw = r & 7;
+    float* xf = &sh->xf[warp][0][0];
+    for (int kt = 0; kt < nkt; ++kt, rp.next(GU4_S)) {
+        const int slot = rp.slot;
+        if (!mbar_wait_abort(&sh->full[slot], rp.par, &sh->abort)) continue;
+        const GU4Stage<RT>& st = ring[slot];
+        {  // this warp's blocks of x -> FP32: lane = (token, 4 * LPR K elements)
+            constexpr int KL = 4 * LPR;
+            const int t = lane >> 3, k = (lane & 7) * KL;
+            if (t < NT) {
+#pragma unroll
+                for (int q = 0; q < LPR; ++q) {
+                    const uint2 xv = *reinterpret_cast<const uint2*>(&st.x[t][warp * KW + k + 4 * q]);
+                    const float2 lo = bf16x2_to_float2(xv.x), hi = bf16x2_to_float2(xv.y);
+                    *reinterpret_cast<float4*>(xf + t * KW + k + 4 * q) = make_float4(lo.x, lo.y, hi.x, hi.y);
+                }
+            }
+        }
+        __syncwarp();
+        const float* xl = xf + hb * 32;
+        float2 part[2][NT];
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {  // two 16-byte chunks = this lane's 32 K elements
+            uint4 wv[2];
+#pragma unroll
+            for (int p = 0; p < 2; ++p)
+                wv[p] = *reinterpret_cast<const uint4*>(&st.w[p][box][r][((c0 + c2) ^ sw) * 16]);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float2 wq[2][2];
+#pragma unroll
+                for (int p = 0; p < 2; ++p) e4m3x4_to_float((&wv[p].x)[q4], wq[p][0], wq[p][1]);
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    const float4 xv = *reinterpret_cast<const float4*>(xl + t * KW + c2 * 16 + q4 * 4);
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        if (c2 == 0 && q4 == 0)
+                            part[p][t] = __fmul2_rn(make_float2(xv.x, xv.y), wq[p][0]);
+                        else
+                            part[p][t] = __ffma2_rn(make_float2(xv.x, xv.y), wq[p][0], part[p][t]);
+                        part[p][t] = __ffma2_rn(make_float2(xv.z, xv.w), wq[p][1], part[p][t]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const float sc = e8m0_to_float(st.sc[p][r][blk]);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) acc[p][t] = __ffma2_rn(part[p][t], make_float2(sc, sc), acc[p][t]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->empty[slot]);
+    }
+    // this warp's partial dots (the lanes of a row add theirs, lower block
+    // first) -> shared memory, double-buffered by group parity so one
+    // barrier per group suffices; then two threads per (token, row) add the
+    // warps' gate and up partials in a fixed order
+    float(*part)[2][TC][RT] = sh->part[grp & 1];
+#pragma unroll
+    for (int p = 0; p < 2; ++p)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            float v = acc[p][t].x + acc[p][t].y;
+            if (LPR == 2) {
+                const float o = __shfl_xor_sync(FULL_MASK, v, 16);
+                v = hb ? o + v : v + o;
+            }
+            if (lane < RT) part[warp][p][t][lane] = v;
+        }
+    consumer_sync<CW * 32>();
+    const int idx = warp * 32 + lane;
+    if (warp < (2 * RT * NT + 31) / 32) {
+        const int pj = idx & 1, rr = (idx >> 1) % RT, t = (idx >> 1) / RT;
+        float v = 0.f;
+        if (t < NT) {
+#pragma unroll
+            for (int w = 0; w < CW; ++w) v += part[w][pj][t][rr];
+        }
+        const float up = __shfl_xor_sync(FULL_MASK, v, 1);
+        if (pj == 0 && t < NT && !sh->abort) {
+            const float hv = v / (1.0f + expf(-v)) * up;
+            int hrow = hs[0];
+#pragma unroll
+            for (int tt = 1; tt < NT; ++tt)
+                if (tt == t) hrow = hs[tt];
+            a.h[(size_t)hrow * s.I + n0 + rr] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+        }
+    }
+}
+
+template <int RT, int CW>
+__global__ void __launch_bounds__((CW + 1) * 32, RT == 32 ? 1 : 2)
+    gate_up_v4_kernel(GateUpArgs a, const __grid_constant__ GU4Maps maps) {
+    constexpr int S = GU4_S;
+    extern __shared__ __align__(128) int smem_i[];
+    const DecodeShape s = a.s;
+    const RouteMap m = carve_map(smem_i, s, false);
+    // swizzled tensor copies want 1024-byte aligned boxes: align at run time
+    // (the launch reserves 1024 spare bytes)
+    const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_i) + gu4_ring_offset(s);
+    GU4Stage<RT>* ring = reinterpret_cast<GU4Stage<RT>*>((raw + 1023) & ~uintptr_t(1023));
+    GU4Shared<RT, CW>* sh = reinterpret_cast<GU4Shared<RT, CW>*>(ring + S);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&sh->full[i], 1);
+            mbar_init(&sh->empty[i], CW);
+        }
+        sh->abort = 0;
+        mbar_init_fence();
+    }
+    build_route_map(m, a.ids, nullptr, s, a.err);  // ends with __syncthreads
+    asm volatile("griddepcontrol.launch_dependents;");
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int KS = s.k + s.S;
+    const int rbs = s.I / RT;
+    const int tiles = m.hdr[0] * rbs;
+    const int nkt = s.d / GU4_KT;
+
+    if (warp == CW) {
+        // ---------------- producer ----------------
+        const uint64_t pol = l2_evict_first_policy();
+        uint32_t it = 0;  // stages issued so far
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+            const int u = tile / rbs;
+            const int n0 = (tile - u * rbs) * RT;
+            const int e = m.uexp[u];
+            const int shx = e >= s.E ? 1 : 0;
+            const int row0 = (shx ? 0 : e) * s.I + n0;
+            const int s0 = m.uoff[u], s1 = m.uoff[u + 1];
+            for (int t0 = s0; t0 < s1 && ok; t0 += TC) {
+                const int nt = min(TC, s1 - t0);
+                const uint16_t* xrow = a.x + (size_t)(lane < nt ? m.hrow[t0 + lane] / KS : 0) * s.d;
+                for (int kt = 0; kt < nkt; ++kt, ++it) {
+                    const int slot = it % S;
+                    if (it >= (uint32_t)S &&
+                        !mbar_wait_abort(&sh->empty[slot], ((it / S) - 1) & 1, &sh->abort)) {
+                        ok = false;
+                        break;
+                    }
+                    GU4Stage<RT>& st = ring[slot];
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&sh->full[slot], 2 * RT * (GU4_KT + GU4_KT / 32) + nt * GU4_KT * 2);
+                        fence_proxy_async();
+#pragma unroll
+                        for (int p = 0; p < 2; ++p) {
+#pragma unroll
+                            for (int b = 0; b < GU4_KT / GU4_BOX; ++b)
+                                tma_2d(st.w[p][b], &maps.w[shx][p], kt * GU4_KT + b * GU4_BOX, row0, &sh->full[slot],
+                                       pol);
+                            tma_2d(st.sc[p], &maps.s[shx][p], kt * (GU4_KT / 32), row0, &sh->full[slot], pol);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane < nt) {
+                        fence_proxy_async();
+                        bulk_g2s_keep(st.x[lane], xrow + (size_t)kt * GU4_KT, GU4_KT * 2, &sh->full[slot]);
+                    }
+                }
+            }
+        }
+        // never leave the CTA with a copy in flight: wait for the last stages
+        for (uint32_t j = it > (uint32_t)S ? it - S : 0; j < it; ++j) mbar_wait(&sh->full[j % S], (j / S) & 1);
+    } else {
+        // ---------------- consumers ----------------
+        RingPos rp{0, 0u};
+        int grp = 0;
+        for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+            const int u = tile / rbs;
+            const int n0 = (tile - u * rbs) * RT;
+            const int s0 = m.uoff[u], s1 = m.uoff[u + 1];
+            for (int t0 = s0; t0 < s1; t0 += TC, ++grp) {
+                const int nt = min(TC, s1 - t0);
+                const int* hs = m.hrow + t0;
+                switch (nt) {
+                    case 1: gu4_group<RT, CW, 1>(a, ring, sh, rp, grp, nkt, warp, lane, n0, hs); break;
+                    case 2: gu4_group<RT, CW, 2>(a, ring, sh, rp, grp, nkt, warp, lane, n0, hs); break;
+                    case 3: gu4_group<RT, CW, 3>(a, ring, sh, rp, grp, nkt, warp, lane, n0, hs); break;
+                    default: gu4_group<RT, CW, 4>(a, ring, sh, rp, grp, nkt, warp, lane, n0, hs); break;
+                }
+            }
+        }
+    }
+    if (lane == 0 && sh->abort) atomicOr(a.err, MOE_DEVERR_TIMEOUT);
+}
+
 // ------------------------------------------------------------ down v2 ----
 // The CTA owns RT output rows and keeps one FP32 accumulator per (row,
 // token) in shared memory.  Its warps split the rows and the distinct
@@ -1724,10 +2015,10 @@ static EncodeTiledFn encode_tiled() {
 // (address, rows, cols, box) so repeated calls on the same weights do not
 // re-encode.
 static bool map_2d_u8(CUtensorMap* out, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
-                      uint32_t box_cols) {
+                      uint32_t box_cols, bool swizzle128 = false) {
     static std::mutex mu;
-    static std::map<std::tuple<const void*, uint64_t, uint64_t, uint32_t, uint32_t>, CUtensorMap> cache;
-    const auto key = std::make_tuple(base, rows, cols, box_rows, box_cols);
+    static std::map<std::tuple<const void*, uint64_t, uint64_t, uint32_t, uint32_t, bool>, CUtensorMap> cache;
+    const auto key = std::make_tuple(base, rows, cols, box_rows, box_cols, swizzle128);
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) {
@@ -1742,7 +2033,8 @@ static bool map_2d_u8(CUtensorMap* out, const void* base, uint64_t rows, uint64_
     const cuuint32_t es[2] = {1, 1};
     CUtensorMap m;
     if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
     if (cache.size() > 1024) cache.clear();
@@ -1797,6 +2089,79 @@ static cudaError_t launch_gate_up_v3(const GateUpArgs& a, const GU3Maps& maps, c
     return cudaGetLastError();
 }
 
+// gate/up v4: K in 512-element stages, RT-row tiles, the whole scale row of
+// a stage in one 16-byte box; scale and weight bases 16-byte aligned.
+#ifndef MOEDEC_GU4_RT
+#define MOEDEC_GU4_RT 16
+#endif
+constexpr int GU4_HOST_RT = MOEDEC_GU4_RT;
+constexpr int GU4_HOST_CW = GU4_HOST_RT == 32 ? 16 : 8;
+
+static bool gate_up_v4_ok(const GateUpArgs& a) {
+    const DecodeShape& s = a.s;
+    if (s.d % GU4_KT || s.I % GU4_HOST_RT) return false;
+    if (!aligned16(a.wg.w) || !aligned16(a.wu.w) || !aligned16(a.wg.s) || !aligned16(a.wu.s)) return false;
+    if (s.S && (!aligned16(a.shg.w) || !aligned16(a.shu.w) || !aligned16(a.shg.s) || !aligned16(a.shu.s)))
+        return false;
+    return true;
+}
+
+static size_t gate_up_v4_smem(const DecodeShape& s) {
+    return gu4_ring_offset(s) + 1024 + (size_t)GU4_S * sizeof(GU4Stage<GU4_HOST_RT>) +
+           sizeof(GU4Shared<GU4_HOST_RT, GU4_HOST_CW>);
+}
+
+static bool gate_up_v4_maps(const GateUpArgs& a, GU4Maps* maps) {
+    const DecodeShape& s = a.s;
+    const MXView v[2][2] = {{a.wg, a.wu}, {a.shg, a.shu}};
+    for (int sh = 0; sh < 2; ++sh) {
+        for (int p = 0; p < 2; ++p) {
+            const MXView& m = sh && !s.S ? v[0][p] : v[sh][p];  // no shared expert: any valid map
+            const uint64_t r = (uint64_t)(sh && s.S ? 1 : s.E) * s.I;
+            if (!map_2d_u8(&maps->w[sh][p], m.w, r, s.d, GU4_HOST_RT, GU4_BOX, true)) return false;
+            if (!map_2d_u8(&maps->s[sh][p], m.s, r, s.d / 32, GU4_HOST_RT, GU4_KT / 32)) return false;
+        }
+    }
+    return true;
+}
+
+// Resident CTAs per SM (0 when the kernel cannot be resident).
+static int gate_up_v4_occupancy(size_t smem, int dev) {
+    static std::mutex mu;
+    static int occ_cache[64] = {0};
+    static size_t smem_cache[64] = {0};
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 64 && smem_cache[dev] == smem) return occ_cache[dev];
+    auto* fn = gate_up_v4_kernel<GU4_HOST_RT, GU4_HOST_CW>;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    int bps = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, fn, (GU4_HOST_CW + 1) * 32, smem) != cudaSuccess) {
+        cudaGetLastError();
+        bps = 0;
+    }
+    if (dev < 64) {
+        occ_cache[dev] = bps;
+        smem_cache[dev] = smem;
+    }
+    return bps;
+}
+
+static cudaError_t launch_gate_up_v4(const GateUpArgs& a, const GU4Maps& maps, size_t smem, int bps,
+                                     const DeviceInfo& di, cudaStream_t st) {
+    const long tiles = (long)max_unique(a.s) * (a.s.I / GU4_HOST_RT);
+    long grid = std::min<long>((long)di.sm_count * bps, tiles);
+    if (grid < 1) grid = 1;
+    gate_up_v4_kernel<GU4_HOST_RT, GU4_HOST_CW><<<(unsigned)grid, (GU4_HOST_CW + 1) * 32, smem, st>>>(a, maps);
+    return cudaGetLastError();
+}
+
+#ifndef MOEDEC_GU4_MIN_TOKENS
+#define MOEDEC_GU4_MIN_TOKENS 2
+#endif
+
 cudaError_t launch_gate_up(const DecodeShape& s, const void* x, const int32_t* ids, MXView wg,
                            MXView wu, MXView shg, MXView shu, void* h, cudaStream_t st) {
     DeviceInfo di;
@@ -1805,6 +2170,14 @@ cudaError_t launch_gate_up(const DecodeShape& s, const void* x, const int32_t* i
     int dev = 0;
     cudaGetDevice(&dev);
     GateUpArgs a{s, (const uint16_t*)x, ids, wg, wu, shg, shu, (uint16_t*)h, di.err_word};
+#ifndef MOEDEC_NO_GU4
+    if (s.B >= MOEDEC_GU4_MIN_TOKENS && gate_up_v4_ok(a)) {
+        const size_t smem = gate_up_v4_smem(s);
+        GU4Maps maps;
+        const int bps = smem <= (size_t)di.max_smem_optin ? gate_up_v4_occupancy(smem, dev) : 0;
+        if (bps >= 1 && gate_up_v4_maps(a, &maps)) return launch_gate_up_v4(a, maps, smem, bps, di, st);
+    }
+#endif
 #ifndef MOEDEC_NO_GU3
     if (gate_up_v3_ok(a) && gate_up_v3_smem(s) <= (size_t)di.max_smem_optin) {
         GU3Maps maps;
