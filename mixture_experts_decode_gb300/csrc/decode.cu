@@ -736,6 +736,15 @@ struct GU3Maps {
     CUtensorMap s[2][2];  // the same for the scales, box 16 rows x 16 B
 };
 
+__device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar,
+                                       uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "l"(pol)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
                                        uint64_t pol) {
     asm volatile(
@@ -982,8 +991,10 @@ struct GU4Shared {
 };
 
 struct GU4Maps {
-    CUtensorMap w[2][2];  // [routed / shared][gate / up], box RT rows x 128 B, 128-byte swizzle
+    CUtensorMap w[2][2];  // [routed / shared][gate / up]: 128-byte swizzle; 2D box RT rows x 128 B,
+                          // or (w3d) 3D box of the stage's 4 column blocks x RT rows x 128 B
     CUtensorMap s[2][2];  // the same for the scales, box RT rows x 16 B
+    int w3d;
 };
 
 // Bounded wait that also gives up as soon as another warp raised `abort`;
@@ -1190,10 +1201,15 @@ __global__ void __launch_bounds__((CW + 1) * 32, RT == 32 ? 1 : 2)
                         fence_proxy_async();
 #pragma unroll
                         for (int p = 0; p < 2; ++p) {
-#pragma unroll
-                            for (int b = 0; b < GU4_KT / GU4_BOX; ++b)
-                                tma_2d(st.w[p][b], &maps.w[shx][p], kt * GU4_KT + b * GU4_BOX, row0, &sh->full[slot],
+                            if (maps.w3d) {
+                                tma_3d(st.w[p][0], &maps.w[shx][p], 0, row0, kt * (GU4_KT / GU4_BOX), &sh->full[slot],
                                        pol);
+                            } else {
+#pragma unroll
+                                for (int b = 0; b < GU4_KT / GU4_BOX; ++b)
+                                    tma_2d(st.w[p][b], &maps.w[shx][p], kt * GU4_KT + b * GU4_BOX, row0,
+                                           &sh->full[slot], pol);
+                            }
                             tma_2d(st.sc[p], &maps.s[shx][p], kt * (GU4_KT / 32), row0, &sh->full[slot], pol);
                         }
                     }
@@ -1899,6 +1915,298 @@ __global__ void __launch_bounds__(DN4_THREADS, 2) down_v4_kernel(DownArgs a) {
     if (!ok && lane == 0) atomicOr(a.err, MOE_DEVERR_TIMEOUT);
 }
 
+// ------------------------------------------------------------ down v5 ----
+// Lane per output row.  A CTA owns a block of RT <= 16 output rows; the
+// stages are (distinct expert, group of up to TC tokens, K slab of KSLAB
+// elements) in order, each holding the expert's RT x KSLAB code block of
+// W_down as 128-byte tensor boxes in the 128-byte swizzled layout, its
+// scale bytes, and the tokens' KSLAB-long slices of h.  The eight consumer
+// warps split each slab evenly (warp w takes its w-th eighth), and in a
+// warp the two lanes r and r + 16 share row r, each taking half of the
+// warp's 16-byte chunks: a lane dequantises its chunk of its row, takes
+// the tokens' h values of that chunk from a per-warp FP32 copy (converted
+// once per stage) as broadcasts, and scales each chunk's partial sum once.
+// After an expert's last slab the two lanes of a row add their halves by a
+// shuffle and the row's lane adds w * dot into the warp's own FP32 partial
+// outputs [token][row] in shared memory, in stage order.  When the block is
+// done the eight warps' partials are added in a fixed order (and, for a
+// two-CTA cluster that splits the experts, the two CTAs' sums in rank
+// order through distributed shared memory) and rounded once to BF16.  With
+// CL = 1 a CTA may own several row blocks in turn.  Every wait is bounded;
+// a wait that runs out raises a CTA-wide abort flag so that all warps still
+// pass every barrier.
+
+constexpr int DN5_CW = 8;
+constexpr int DN5_THREADS = (DN5_CW + 1) * 32;
+constexpr int DN5_RTMAX = 16;
+constexpr int DN5_SMAX = 6;
+
+struct DN5Maps {
+    CUtensorMap w[2];  // [routed / shared]: box RT rows x 128 B, 128-byte swizzle
+    CUtensorMap s[2];  // scales, box RT rows x 16 B (used when the slab is shorter than I)
+};
+
+struct DN5Params {
+    int RT;           // rows per block (even, <= 16)
+    int KSLAB;        // K elements per stage: I itself (<= 768) or 512
+    int S;            // ring stages
+    int nblk;         // row blocks
+    int scale2d;      // 1: scales by a 2D tensor copy (KSLAB = 512 < I); 0: one 1D copy (KSLAB = I)
+    int stage_bytes;  // stage layout: weights at 0 (KSLAB / 128 box slots of 2 KB), scales, h
+    int sc_off, h_off;
+};
+
+template <int NT>
+__device__ __forceinline__ void dn5_group(const DN5Params& P, const char* ring, uint64_t* full, uint64_t* empty,
+                                          int* abortf, RingPos& rp, int nslab, int warp, int lane, float* xf,
+                                          float* yp, const int* tok, const float* wt, int rows) {
+    const int KSLAB = P.KSLAB;
+    const int KW = KSLAB / 8;     // K elements of a warp per stage
+    const int CPL = KSLAB / 256;  // 16-byte chunks of a lane per stage
+    const int r = lane & 15, hb = lane >> 4;
+    float2 acc[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t] = make_float2(0.f, 0.f);
+    for (int sl = 0; sl < nslab; ++sl, rp.next(P.S)) {
+        if (!mbar_wait_abort(&full[rp.slot], rp.par, abortf)) continue;
+        const char* st = ring + (size_t)rp.slot * P.stage_bytes;
+        {  // this warp's part of the tokens' h -> FP32: lane = (token, KW / 8 elements)
+            const uint16_t* hst = reinterpret_cast<const uint16_t*>(st + P.h_off);
+            const int t = lane >> 3, k = (lane & 7) * (KW / 8);
+            if (t < NT) {
+                for (int q = 0; q < KW / 32; ++q) {
+                    const uint2 hv = *reinterpret_cast<const uint2*>(hst + t * KSLAB + warp * KW + k + 4 * q);
+                    const float2 lo = bf16x2_to_float2(hv.x), hi = bf16x2_to_float2(hv.y);
+                    *reinterpret_cast<float4*>(xf + t * KW + k + 4 * q) = make_float4(lo.x, lo.y, hi.x, hi.y);
+                }
+            }
+        }
+        __syncwarp();
+        const uint8_t* scs = reinterpret_cast<const uint8_t*>(st + P.sc_off) + r * (KSLAB / 32);
+        const int c0 = warp * (KSLAB / 128) + hb * CPL;  // this lane's first chunk in the slab
+        for (int q = 0; q < CPL; ++q) {
+            const int c = c0 + q;
+            const uint4 wv =
+                *reinterpret_cast<const uint4*>(st + (c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+            const float sc = e8m0_to_float(scs[c >> 1]);
+            const float* xl = xf + (hb * CPL + q) * 16;
+            float2 part[NT];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float2 wq[2];
+                e4m3x4_to_float((&wv.x)[q4], wq[0], wq[1]);
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    const float4 xv = *reinterpret_cast<const float4*>(xl + t * KW + q4 * 4);
+                    if (q4 == 0)
+                        part[t] = __fmul2_rn(make_float2(xv.x, xv.y), wq[0]);
+                    else
+                        part[t] = __ffma2_rn(make_float2(xv.x, xv.y), wq[0], part[t]);
+                    part[t] = __ffma2_rn(make_float2(xv.z, xv.w), wq[1], part[t]);
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < NT; ++t) acc[t] = __ffma2_rn(part[t], make_float2(sc, sc), acc[t]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[rp.slot]);
+    }
+    // the expert's dots (lower half of K first) times the routing weights
+    // into this warp's partial outputs
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        float v = acc[t].x + acc[t].y;
+        const float o = __shfl_xor_sync(FULL_MASK, v, 16);
+        v = hb ? o + v : v + o;
+        if (hb == 0 && r < rows) yp[tok[t] * DN5_RTMAX + r] += wt[t] * v;
+    }
+}
+
+template <int CL>
+__global__ void __launch_bounds__(DN5_THREADS, 2)
+    down_v5_kernel(DownArgs a, const __grid_constant__ DN5Maps maps, const DN5Params P) {
+    extern __shared__ __align__(128) int smem_i[];
+    const DecodeShape s = a.s;
+    const RouteMap m = carve_map(smem_i, s, true);
+    const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_i) + map_ints(s, true) * 4;
+    char* ring = reinterpret_cast<char*>((raw + 1023) & ~uintptr_t(1023));
+    const int S = P.S, KSLAB = P.KSLAB, RT = P.RT;
+    float* xfa = reinterpret_cast<float*>(ring + (size_t)S * P.stage_bytes);  // [CW][TC][KSLAB / 8]
+    float* ypa = xfa + DN5_CW * TC * (KSLAB / 8);                               // [CW][B][RTMAX]
+    uint64_t* full = reinterpret_cast<uint64_t*>(ypa + (size_t)DN5_CW * s.B * DN5_RTMAX);
+    uint64_t* empty = full + S;
+    int* abortf = reinterpret_cast<int*>(empty + S);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], DN5_CW);
+        }
+        *abortf = 0;
+        mbar_init_fence();
+    }
+    build_route_map(m, a.ids, a.w, s, a.err, true);  // ends with __syncthreads
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = CL > 1 ? (int)cluster_rank() : 0;
+    const int nu = m.hdr[0];
+    const int nslab = s.I / KSLAB;
+    const int cl_idx = blockIdx.x / CL;
+    const int step = CL > 1 ? P.nblk : (int)gridDim.x;  // row blocks advance (CL > 1: one block)
+
+    if (warp == DN5_CW) {
+        // ---------------- producer ----------------
+        const uint64_t pol = l2_evict_first_policy();
+        struct Cur {
+            int rb, u, g0, sl;
+        };
+        auto settle = [&](Cur& c) {  // skip row blocks with no expert for this rank
+            while (c.rb < P.nblk && c.u >= nu) {
+                c.rb += step;
+                c.u = rank;
+            }
+        };
+        auto advance = [&](Cur& c) {
+            if (++c.sl < nslab) return;
+            c.sl = 0;
+            c.g0 += TC;
+            if (c.g0 < m.ucnt[c.u]) return;
+            c.g0 = 0;
+            c.u += CL;
+            if (c.u >= nu) {
+                c.rb += step;
+                c.u = rank;
+            }
+            settle(c);
+        };
+        auto issue_w = [&](const Cur& c, int slot) {
+            const int e = m.uexp[c.u];
+            const int shx = e >= s.E ? 1 : 0;
+            const int o0 = c.rb * RT, rows = min(RT, s.d - o0);
+            const int row0 = (shx ? 0 : e) * s.d + o0;
+            const int nt = min(TC, m.ucnt[c.u] - c.g0);
+            char* st = ring + (size_t)slot * P.stage_bytes;
+            if (lane == 0) {
+                const uint32_t sbytes = P.scale2d ? (uint32_t)RT * 16 : (uint32_t)rows * (s.I / 32);
+                mbar_arrive_expect_tx(&full[slot], (uint32_t)RT * KSLAB + sbytes + nt * KSLAB * 2);
+                fence_proxy_async();
+                for (int bx = 0; bx < KSLAB / 128; ++bx)
+                    tma_2d(st + bx * 2048, &maps.w[shx], c.sl * KSLAB + bx * 128, row0, &full[slot], pol);
+                if (P.scale2d)
+                    tma_2d(st + P.sc_off, &maps.s[shx], c.sl * (KSLAB / 32), row0, &full[slot], pol);
+                else
+                    bulk_g2s(st + P.sc_off, (shx ? a.shd.s : a.wd.s) + (size_t)row0 * (s.I / 32), sbytes, &full[slot],
+                             pol);
+            }
+        };
+        auto issue_h = [&](const Cur& c, int slot) {
+            const int nt = min(TC, m.ucnt[c.u] - c.g0);
+            char* st = ring + (size_t)slot * P.stage_bytes;
+            if (lane < nt) {
+                fence_proxy_async();
+                bulk_g2s_keep(st + P.h_off + (size_t)lane * KSLAB * 2,
+                              a.h + (size_t)m.hrow[m.uoff[c.u] + c.g0 + lane] * s.I + (size_t)c.sl * KSLAB,
+                              KSLAB * 2, &full[slot]);
+            }
+        };
+        // the weights of the first S stages go out before waiting for the
+        // gate/up pass (they do not depend on it), their h after
+        Cur pw{cl_idx, rank, 0, 0};
+        settle(pw);
+        int npro = 0;
+        for (; npro < S && pw.rb < P.nblk; ++npro) {
+            issue_w(pw, npro);
+            advance(pw);
+        }
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        {
+            Cur ph{cl_idx, rank, 0, 0};
+            settle(ph);
+            for (int i = 0; i < npro; ++i) {
+                issue_h(ph, i);
+                advance(ph);
+            }
+        }
+        uint32_t issued = npro;
+        RingPos rp{0, 0u};  // reached only when npro == S
+        while (pw.rb < P.nblk) {
+            if (!mbar_wait_abort(&empty[rp.slot], rp.par, abortf)) break;
+            issue_w(pw, rp.slot);
+            __syncwarp();
+            issue_h(pw, rp.slot);
+            advance(pw);
+            ++issued;
+            rp.next(S);
+        }
+        // never leave the CTA with a copy in flight
+        for (uint32_t j = issued > (uint32_t)S ? issued - S : 0; j < issued; ++j)
+            mbar_wait(&full[j % S], (j / S) & 1);
+    } else {
+        // ---------------- consumers ----------------
+        float* yp = ypa + (size_t)warp * s.B * DN5_RTMAX;
+        float* xf = xfa + warp * TC * (KSLAB / 8);
+        RingPos rp{0, 0u};
+        for (int rb = cl_idx; rb < P.nblk; rb += step) {
+            const int o0 = rb * RT, rows = min(RT, s.d - o0);
+            for (int i = lane; i < s.B * DN5_RTMAX; i += 32) yp[i] = 0.f;
+            __syncwarp();
+            for (int u = rank; u < nu; u += CL) {
+                const int cnt = m.ucnt[u], s0 = m.uoff[u];
+                for (int g0 = 0; g0 < cnt; g0 += TC) {
+                    const int nt = min(TC, cnt - g0);
+                    const int* tk = m.tok + s0 + g0;
+                    const float* wsp = m.wt + s0 + g0;
+                    switch (nt) {
+                        case 1: dn5_group<1>(P, ring, full, empty, abortf, rp, nslab, warp, lane, xf, yp, tk, wsp, rows); break;
+                        case 2: dn5_group<2>(P, ring, full, empty, abortf, rp, nslab, warp, lane, xf, yp, tk, wsp, rows); break;
+                        case 3: dn5_group<3>(P, ring, full, empty, abortf, rp, nslab, warp, lane, xf, yp, tk, wsp, rows); break;
+                        default: dn5_group<4>(P, ring, full, empty, abortf, rp, nslab, warp, lane, xf, yp, tk, wsp, rows); break;
+                    }
+                }
+            }
+            if (CL == 1) {
+                // add the warps' partials in a fixed order, round once to BF16
+                consumer_sync<DN5_CW * 32>();
+                for (int i = threadIdx.x; i < s.B * RT; i += DN5_CW * 32) {
+                    const int b = i / RT, rr = i - b * RT;
+                    if (rr < rows) {
+                        float v = 0.f;
+#pragma unroll
+                        for (int w = 0; w < DN5_CW; ++w) v += ypa[((size_t)w * s.B + b) * DN5_RTMAX + rr];
+                        a.y[(size_t)b * s.d + o0 + rr] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+                    }
+                }
+                consumer_sync<DN5_CW * 32>();
+            }
+        }
+    }
+    if (CL > 1) {
+        // one row block per cluster: the warps' partials, then the ranks' sums
+        // in rank order; CTA `rank` stores rows [rank * RT / CL, (rank + 1) * RT / CL)
+        __syncthreads();
+        const int o0 = cl_idx * RT, rows = min(RT, s.d - o0);
+        for (int i = threadIdx.x; i < s.B * DN5_RTMAX; i += DN5_THREADS) {
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < DN5_CW; ++w) v += ypa[(size_t)w * s.B * DN5_RTMAX + i];
+            ypa[i] = v;
+        }
+        cluster_sync_all();
+        const int RR = RT / CL;
+        for (int i = threadIdx.x; i < s.B * RR; i += DN5_THREADS) {
+            const int b = i / RR, rl = rank * RR + (i - b * RR);
+            if (rl < rows) {
+                const float* p = ypa + (size_t)b * DN5_RTMAX + rl;
+                float v = 0.f;
+#pragma unroll
+                for (int q = 0; q < CL; ++q) v += ld_cluster_f32(p, q);
+                a.y[(size_t)b * s.d + o0 + rl] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+            }
+        }
+        cluster_sync_all();  // keep this CTA's sums alive for its peer
+    }
+    if (lane == 0 && *abortf) atomicOr(a.err, MOE_DEVERR_TIMEOUT);
+}
+
 // -------------------------------------------------------------- host -----
 
 // Lanes per weight row: the largest power of two <= 32 that divides the
@@ -2043,6 +2351,38 @@ static bool map_2d_u8(CUtensorMap* out, const void* base, uint64_t rows, uint64_
     return true;
 }
 
+// 3D uint8 tensor map viewing a [rows][cols] matrix as [cols / 128][rows][128]
+// (128-byte column blocks): one copy of a box (128, box_rows, nblk) brings
+// box_rows rows x nblk * 128 bytes as nblk consecutive [box_rows][128] tiles,
+// each in the 128-byte swizzled layout.  Cached like map_2d_u8.
+static bool map_3d_u8_blocks(CUtensorMap* out, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                             uint32_t nblk) {
+    static std::mutex mu;
+    static std::map<std::tuple<const void*, uint64_t, uint64_t, uint32_t, uint32_t>, CUtensorMap> cache;
+    const auto key = std::make_tuple(base, rows, cols, box_rows, nblk);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+        *out = it->second;
+        return true;
+    }
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn || cols % 128) return false;
+    const cuuint64_t dims[3] = {128, rows, cols / 128};
+    const cuuint64_t strides[2] = {cols, 128};
+    const cuuint32_t box[3] = {128, box_rows, nblk};
+    const cuuint32_t es[3] = {1, 1, 1};
+    CUtensorMap m;
+    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    if (cache.size() > 1024) cache.clear();
+    cache[key] = m;
+    *out = m;
+    return true;
+}
+
 static bool gate_up_v3_maps(const GateUpArgs& a, GU3Maps* maps) {
     const DecodeShape& s = a.s;
     const MXView v[2][2] = {{a.wg, a.wu}, {a.shg, a.shu}};
@@ -2111,18 +2451,32 @@ static size_t gate_up_v4_smem(const DecodeShape& s) {
            sizeof(GU4Shared<GU4_HOST_RT, GU4_HOST_CW>);
 }
 
+#ifndef MOEDEC_GU4_W3D
+#define MOEDEC_GU4_W3D 1
+#endif
+
 static bool gate_up_v4_maps(const GateUpArgs& a, GU4Maps* maps) {
     const DecodeShape& s = a.s;
     const MXView v[2][2] = {{a.wg, a.wu}, {a.shg, a.shu}};
-    for (int sh = 0; sh < 2; ++sh) {
-        for (int p = 0; p < 2; ++p) {
-            const MXView& m = sh && !s.S ? v[0][p] : v[sh][p];  // no shared expert: any valid map
-            const uint64_t r = (uint64_t)(sh && s.S ? 1 : s.E) * s.I;
-            if (!map_2d_u8(&maps->w[sh][p], m.w, r, s.d, GU4_HOST_RT, GU4_BOX, true)) return false;
-            if (!map_2d_u8(&maps->s[sh][p], m.s, r, s.d / 32, GU4_HOST_RT, GU4_KT / 32)) return false;
+    // one 3D copy per projection and stage when the driver takes the block
+    // view, else four 2D copies
+    maps->w3d = MOEDEC_GU4_W3D;
+    for (int pass = 0; pass < 2; ++pass) {
+        bool ok = true;
+        for (int sh = 0; sh < 2 && ok; ++sh) {
+            for (int p = 0; p < 2 && ok; ++p) {
+                const MXView& m = sh && !s.S ? v[0][p] : v[sh][p];  // no shared expert: any valid map
+                const uint64_t r = (uint64_t)(sh && s.S ? 1 : s.E) * s.I;
+                ok = maps->w3d ? map_3d_u8_blocks(&maps->w[sh][p], m.w, r, s.d, GU4_HOST_RT, GU4_KT / GU4_BOX)
+                               : map_2d_u8(&maps->w[sh][p], m.w, r, s.d, GU4_HOST_RT, GU4_BOX, true);
+                ok = ok && map_2d_u8(&maps->s[sh][p], m.s, r, s.d / 32, GU4_HOST_RT, GU4_KT / 32);
+            }
         }
+        if (ok) return true;
+        if (!maps->w3d) return false;
+        maps->w3d = 0;
     }
-    return true;
+    return false;
 }
 
 // Resident CTAs per SM (0 when the kernel cannot be resident).
@@ -2397,6 +2751,147 @@ static cudaError_t launch_down_v4_rw(const DownArgs& a, size_t smem, int dev, in
     }
 }
 
+// ---- down v5 plan: slab, stage layout, ring depth, row block and cluster
+#ifndef MOEDEC_DN5_MAXB
+#define MOEDEC_DN5_MAXB 64
+#endif
+
+struct DN5Plan {
+    DN5Params P;
+    int CL, grid;
+    size_t smem;
+};
+
+static int smem_per_sm(int dev) {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 64 && cache[dev]) return cache[dev];
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        v = 0;
+    }
+    if (dev < 64) cache[dev] = v;
+    return v;
+}
+
+static bool down_v5_plan(const DownArgs& a, const DeviceInfo& di, int dev, DN5Plan* out) {
+    const DecodeShape& s = a.s;
+    if (s.B > MOEDEC_DN5_MAXB || s.I % 256 || s.d % 2) return false;
+    DN5Params P{};
+    if (s.I <= 768) {
+        P.KSLAB = s.I;
+        P.scale2d = 0;
+    } else if (s.I % 512 == 0) {
+        P.KSLAB = 512;
+        P.scale2d = 1;
+    } else {
+        return false;
+    }
+    if (!aligned16(a.wd.w) || !aligned16(a.wd.s)) return false;
+    if (s.S && (!aligned16(a.shd.w) || !aligned16(a.shd.s))) return false;
+    auto r128 = [](size_t v) { return (v + 127) / 128 * 128; };
+    auto r1024 = [](size_t v) { return (v + 1023) / 1024 * 1024; };
+    P.sc_off = P.KSLAB * 16;
+    P.h_off = (int)(P.sc_off + r128((size_t)DN5_RTMAX * (P.KSLAB / 32)));
+    P.stage_bytes = (int)r1024((size_t)P.h_off + (size_t)TC * P.KSLAB * 2);
+    const size_t fixed = map_ints(s, true) * 4 + 1024 + (size_t)DN5_CW * TC * (P.KSLAB / 8) * 4 +
+                         (size_t)DN5_CW * s.B * DN5_RTMAX * 4 + 2 * DN5_SMAX * 8 + 16;
+    // two CTAs per SM
+    const int per_sm = smem_per_sm(dev);
+    const size_t limit = per_sm > 0 ? (size_t)per_sm / 2 - 1024 : 0;
+    if (limit <= fixed) return false;
+    P.S = (int)std::min<size_t>(DN5_SMAX, (limit - fixed) / P.stage_bytes);
+    if (P.S < 3) return false;
+    const size_t smem = fixed + (size_t)P.S * P.stage_bytes;
+    if (smem > (size_t)di.max_smem_optin) return false;
+    // row block and cluster: the fewest rows per CTA over the waves the
+    // grid needs (two CTAs per SM), preferring larger blocks on ties
+    const int slots = 2 * di.sm_count;
+    const int nu_max = max_unique(s);
+    int best_cost = 1 << 30, bRT = 0, bCL = 0;
+    for (int CL = 2; CL >= 1; --CL) {
+        if (CL > nu_max) continue;
+        for (int RT = DN5_RTMAX; RT >= 8; RT -= 2) {
+            const int nblk = (s.d + RT - 1) / RT;
+            int cost;
+            if (CL > 1) {
+                if (nblk * CL > slots) continue;
+                cost = RT * 64 / CL;
+            } else {
+                const int ctas = std::min(nblk, slots);
+                const int waves = (nblk + ctas - 1) / ctas;
+                cost = waves * RT * 64;
+            }
+            if (cost < best_cost) {
+                best_cost = cost;
+                bRT = RT;
+                bCL = CL;
+            }
+        }
+    }
+    if (!bRT) return false;
+    P.RT = bRT;
+    P.nblk = (s.d + bRT - 1) / bRT;
+    out->P = P;
+    out->CL = bCL;
+    out->grid = bCL > 1 ? P.nblk * bCL : std::min(P.nblk, slots);
+    out->smem = smem;
+    return true;
+}
+
+static bool down_v5_maps(const DownArgs& a, const DN5Params& P, DN5Maps* maps) {
+    const DecodeShape& s = a.s;
+    const MXView v[2] = {a.wd, a.shd};
+    for (int sh = 0; sh < 2; ++sh) {
+        const MXView& m = sh && !s.S ? v[0] : v[sh];  // no shared expert: any valid map
+        const uint64_t rows = (uint64_t)(sh && s.S ? 1 : s.E) * s.d;
+        if (!map_2d_u8(&maps->w[sh], m.w, rows, s.I, P.RT, 128, true)) return false;
+        if (P.scale2d && !map_2d_u8(&maps->s[sh], m.s, rows, s.I / 32, P.RT, 16)) return false;
+        if (!P.scale2d) maps->s[sh] = maps->w[sh];  // unused
+    }
+    return true;
+}
+
+template <int CL>
+static cudaError_t launch_down_v5_k(const DownArgs& a, const DN5Maps& maps, const DN5Plan& pl, int dev,
+                                    cudaStream_t st, bool pdl) {
+    static std::mutex mu;
+    static size_t attr_smem[64] = {0};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= 64 || attr_smem[dev] < pl.smem) {
+            cudaError_t err = cudaFuncSetAttribute(down_v5_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)std::max<size_t>(pl.smem, 48 * 1024));
+            if (err != cudaSuccess) return err;
+            if (dev < 64) attr_smem[dev] = pl.smem;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid);
+    cfg.blockDim = dim3(DN5_THREADS);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (CL > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = CL;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, down_v5_kernel<CL>, a, maps, pl.P);
+}
+
 cudaError_t launch_down(const DecodeShape& s, const void* h, const int32_t* ids, const float* w,
                         MXView wd, MXView shd, void* y, cudaStream_t st, bool after_gate_up) {
     DeviceInfo di;
@@ -2405,6 +2900,16 @@ cudaError_t launch_down(const DecodeShape& s, const void* h, const int32_t* ids,
     int dev = 0;
     cudaGetDevice(&dev);
     DownArgs a{s, (const uint16_t*)h, ids, w, wd, shd, (uint16_t*)y, di.err_word, 1};
+#ifdef MOEDEC_DN5
+    {
+        DN5Plan pl;
+        DN5Maps maps;
+        if (down_v5_plan(a, di, dev, &pl) && down_v5_maps(a, pl.P, &maps)) {
+            if (pl.CL > 1) return launch_down_v5_k<2>(a, maps, pl, dev, st, after_gate_up);
+            return launch_down_v5_k<1>(a, maps, pl, dev, st, after_gate_up);
+        }
+    }
+#endif
 #ifndef MOEDEC_NO_DN4
     if (down_v3_ok(s, wd, shd)) {
         const int RW = dn4_rw(s.I);
