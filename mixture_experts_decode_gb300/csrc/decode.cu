@@ -1512,7 +1512,7 @@ __host__ __device__ inline size_t dn3_smem_offset(const DecodeShape& s, int RW) 
 #endif
 __host__ __device__ inline int dn3_rw(int I) { return I >= 2048 ? 1 : MOEDEC_DN3_RWSMALL; }
 
-template <int RW, int NT>
+template <int RW, int NT, int NCH = 0>
 __device__ __forceinline__ bool dn3_group(const DownArgs& a, const DN3Layout& L, const char* st, uint64_t* full,
                                           uint64_t* empty, uint32_t parity, int cw, int lane, const int* toks,
                                           const float* ws, int nt, float* acc_rows) {
@@ -1527,7 +1527,8 @@ __device__ __forceinline__ bool dn3_group(const DownArgs& a, const DN3Layout& L,
     for (int r = 0; r < RW; ++r)
 #pragma unroll
         for (int t = 0; t < NT; ++t) acc[r][t] = make_float2(0.f, 0.f);
-    const int nch = s.I / 256;  // 8-byte chunks per lane
+    const int nch = NCH ? NCH : s.I / 256;  // 8-byte chunks per lane
+#pragma unroll(NCH ? NCH : 1)
     for (int i = 0; i < nch; ++i) {
         const int k0 = (lane + 32 * i) * 8;  // first K element of this chunk
         float2 hf[NT][4];  // the tokens' eight activations, converted once for all rows
@@ -1775,7 +1776,7 @@ __device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t ran
     return v;
 }
 
-template <int RW, int CL>
+template <int RW, int CL, int NCH>
 __global__ void __launch_bounds__(DN4_THREADS, 2) down_v4_kernel(DownArgs a) {
     constexpr int RT = DN4_CW * RW;
     extern __shared__ __align__(128) int smem_i[];
@@ -1886,10 +1887,10 @@ __global__ void __launch_bounds__(DN4_THREADS, 2) down_v4_kernel(DownArgs a) {
                 const int* tk = m.tok + s0 + t0;
                 const float* wsp = m.wt + s0 + t0;
                 switch (nt) {
-                    case 1: ok = dn3_group<RW, 1>(a, L, st, &full[slot], &empty[slot], par, warp, lane, tk, wsp, nt, acc_rows); break;
-                    case 2: ok = dn3_group<RW, 2>(a, L, st, &full[slot], &empty[slot], par, warp, lane, tk, wsp, nt, acc_rows); break;
-                    case 3: ok = dn3_group<RW, 3>(a, L, st, &full[slot], &empty[slot], par, warp, lane, tk, wsp, nt, acc_rows); break;
-                    default: ok = dn3_group<RW, 4>(a, L, st, &full[slot], &empty[slot], par, warp, lane, tk, wsp, nt, acc_rows); break;
+                    case 1: ok = dn3_group<RW, 1, NCH>(a, L, st, &full[slot], &empty[slot], par, warp, lane, tk, wsp, nt, acc_rows); break;
+                    case 2: ok = dn3_group<RW, 2, NCH>(a, L, st, &full[slot], &empty[slot], par, warp, lane, tk, wsp, nt, acc_rows); break;
+                    case 3: ok = dn3_group<RW, 3, NCH>(a, L, st, &full[slot], &empty[slot], par, warp, lane, tk, wsp, nt, acc_rows); break;
+                    default: ok = dn3_group<RW, 4, NCH>(a, L, st, &full[slot], &empty[slot], par, warp, lane, tk, wsp, nt, acc_rows); break;
                 }
                 if (++slot == L.S) {
                     slot = 0;
@@ -1942,7 +1943,7 @@ constexpr int DN5_RTMAX = 16;
 constexpr int DN5_SMAX = 6;
 
 struct DN5Maps {
-    CUtensorMap w[2];  // [routed / shared]: box RT rows x 128 B, 128-byte swizzle
+    CUtensorMap w[2];  // [routed / shared]: 3D block view, box 128 B x RT rows x KSLAB / 128 blocks, 128-byte swizzle
     CUtensorMap s[2];  // scales, box RT rows x 16 B (used when the slab is shorter than I)
 };
 
@@ -1956,14 +1957,14 @@ struct DN5Params {
     int sc_off, h_off;
 };
 
-template <int NT>
+template <int KSLAB, int NT>
 __device__ __forceinline__ void dn5_group(const DN5Params& P, const char* ring, uint64_t* full, uint64_t* empty,
                                           int* abortf, RingPos& rp, int nslab, int warp, int lane, float* xf,
                                           float* yp, const int* tok, const float* wt, int rows) {
-    const int KSLAB = P.KSLAB;
-    const int KW = KSLAB / 8;     // K elements of a warp per stage
-    const int CPL = KSLAB / 256;  // 16-byte chunks of a lane per stage
+    constexpr int KW = KSLAB / 8;     // K elements of a warp per stage
+    constexpr int CPL = KSLAB / 256;  // 16-byte chunks of a lane per stage
     const int r = lane & 15, hb = lane >> 4;
+    const int RT = P.RT;
     float2 acc[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[t] = make_float2(0.f, 0.f);
@@ -1974,6 +1975,7 @@ __device__ __forceinline__ void dn5_group(const DN5Params& P, const char* ring, 
             const uint16_t* hst = reinterpret_cast<const uint16_t*>(st + P.h_off);
             const int t = lane >> 3, k = (lane & 7) * (KW / 8);
             if (t < NT) {
+#pragma unroll
                 for (int q = 0; q < KW / 32; ++q) {
                     const uint2 hv = *reinterpret_cast<const uint2*>(hst + t * KSLAB + warp * KW + k + 4 * q);
                     const float2 lo = bf16x2_to_float2(hv.x), hi = bf16x2_to_float2(hv.y);
@@ -1984,10 +1986,14 @@ __device__ __forceinline__ void dn5_group(const DN5Params& P, const char* ring, 
         __syncwarp();
         const uint8_t* scs = reinterpret_cast<const uint8_t*>(st + P.sc_off) + r * (KSLAB / 32);
         const int c0 = warp * (KSLAB / 128) + hb * CPL;  // this lane's first chunk in the slab
+#pragma unroll
         for (int q = 0; q < CPL; ++q) {
+            // the slab's 128-byte column blocks are consecutive [RT][128] tiles in
+            // the 128-byte swizzled layout: chunk j of tile row y sits at chunk
+            // j ^ (y & 7), y counted from the (1024-byte aligned) stage start
             const int c = c0 + q;
-            const uint4 wv =
-                *reinterpret_cast<const uint4*>(st + (c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+            const int y = (c >> 3) * RT + r;
+            const uint4 wv = *reinterpret_cast<const uint4*>(st + y * 128 + (((c & 7) ^ (y & 7)) << 4));
             const float sc = e8m0_to_float(scs[c >> 1]);
             const float* xl = xf + (hb * CPL + q) * 16;
             float2 part[NT];
@@ -2022,7 +2028,7 @@ __device__ __forceinline__ void dn5_group(const DN5Params& P, const char* ring, 
     }
 }
 
-template <int CL>
+template <int CL, int KSLAB>
 __global__ void __launch_bounds__(DN5_THREADS, 2)
     down_v5_kernel(DownArgs a, const __grid_constant__ DN5Maps maps, const DN5Params P) {
     extern __shared__ __align__(128) int smem_i[];
@@ -2030,7 +2036,7 @@ __global__ void __launch_bounds__(DN5_THREADS, 2)
     const RouteMap m = carve_map(smem_i, s, true);
     const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_i) + map_ints(s, true) * 4;
     char* ring = reinterpret_cast<char*>((raw + 1023) & ~uintptr_t(1023));
-    const int S = P.S, KSLAB = P.KSLAB, RT = P.RT;
+    const int S = P.S, RT = P.RT;
     float* xfa = reinterpret_cast<float*>(ring + (size_t)S * P.stage_bytes);  // [CW][TC][KSLAB / 8]
     float* ypa = xfa + DN5_CW * TC * (KSLAB / 8);                               // [CW][B][RTMAX]
     uint64_t* full = reinterpret_cast<uint64_t*>(ypa + (size_t)DN5_CW * s.B * DN5_RTMAX);
@@ -2089,8 +2095,7 @@ __global__ void __launch_bounds__(DN5_THREADS, 2)
                 const uint32_t sbytes = P.scale2d ? (uint32_t)RT * 16 : (uint32_t)rows * (s.I / 32);
                 mbar_arrive_expect_tx(&full[slot], (uint32_t)RT * KSLAB + sbytes + nt * KSLAB * 2);
                 fence_proxy_async();
-                for (int bx = 0; bx < KSLAB / 128; ++bx)
-                    tma_2d(st + bx * 2048, &maps.w[shx], c.sl * KSLAB + bx * 128, row0, &full[slot], pol);
+                tma_3d(st, &maps.w[shx], 0, row0, c.sl * (KSLAB / 128), &full[slot], pol);
                 if (P.scale2d)
                     tma_2d(st + P.sc_off, &maps.s[shx], c.sl * (KSLAB / 32), row0, &full[slot], pol);
                 else
@@ -2156,10 +2161,10 @@ __global__ void __launch_bounds__(DN5_THREADS, 2)
                     const int* tk = m.tok + s0 + g0;
                     const float* wsp = m.wt + s0 + g0;
                     switch (nt) {
-                        case 1: dn5_group<1>(P, ring, full, empty, abortf, rp, nslab, warp, lane, xf, yp, tk, wsp, rows); break;
-                        case 2: dn5_group<2>(P, ring, full, empty, abortf, rp, nslab, warp, lane, xf, yp, tk, wsp, rows); break;
-                        case 3: dn5_group<3>(P, ring, full, empty, abortf, rp, nslab, warp, lane, xf, yp, tk, wsp, rows); break;
-                        default: dn5_group<4>(P, ring, full, empty, abortf, rp, nslab, warp, lane, xf, yp, tk, wsp, rows); break;
+                        case 1: dn5_group<KSLAB, 1>(P, ring, full, empty, abortf, rp, nslab, warp, lane, xf, yp, tk, wsp, rows); break;
+                        case 2: dn5_group<KSLAB, 2>(P, ring, full, empty, abortf, rp, nslab, warp, lane, xf, yp, tk, wsp, rows); break;
+                        case 3: dn5_group<KSLAB, 3>(P, ring, full, empty, abortf, rp, nslab, warp, lane, xf, yp, tk, wsp, rows); break;
+                        default: dn5_group<KSLAB, 4>(P, ring, full, empty, abortf, rp, nslab, warp, lane, xf, yp, tk, wsp, rows); break;
                     }
                 }
             }
@@ -2693,14 +2698,14 @@ static size_t down_v4_smem(const DecodeShape& s, int RW) {
     return dn4_smem_offset(s, RW) + (size_t)L.S * L.stage_bytes + 2 * DN4_SMAX * sizeof(uint64_t) + 128;
 }
 
-template <int RW, int CL>
+template <int RW, int CL, int NCH>
 static cudaError_t launch_down_v4_k(const DownArgs& a, size_t smem, int dev, cudaStream_t st, bool pdl) {
     static std::mutex mu;
     static size_t attr_smem[64] = {0};
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev >= 64 || attr_smem[dev] < smem) {
-            cudaError_t err = cudaFuncSetAttribute(down_v4_kernel<RW, CL>,
+            cudaError_t err = cudaFuncSetAttribute(down_v4_kernel<RW, CL, NCH>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    (int)std::max<size_t>(smem, 48 * 1024));
             if (err != cudaSuccess) return err;
@@ -2729,7 +2734,7 @@ static cudaError_t launch_down_v4_k(const DownArgs& a, size_t smem, int dev, cud
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, down_v4_kernel<RW, CL>, a);
+    return cudaLaunchKernelEx(&cfg, down_v4_kernel<RW, CL, NCH>, a);
 }
 
 // Cluster size: enough CTAs to fill the GPU twice, never more than the
@@ -2741,14 +2746,29 @@ static int dn4_cl(const DecodeShape& s, int RW, int sm_count) {
     return cl;
 }
 
+template <int RW, int NCH>
+static cudaError_t launch_down_v4_cl(const DownArgs& a, size_t smem, int dev, int sm_count, cudaStream_t st,
+                                     bool pdl) {
+    switch (dn4_cl(a.s, RW, sm_count)) {
+        case 1: return launch_down_v4_k<RW, 1, NCH>(a, smem, dev, st, pdl);
+        case 2: return launch_down_v4_k<RW, 2, NCH>(a, smem, dev, st, pdl);
+        default: return launch_down_v4_k<RW, 4, NCH>(a, smem, dev, st, pdl);
+    }
+}
+
+// The chunk loop is unrolled for the common lengths (I = 768 at two rows per
+// warp, I = 2048 at one), a run-time loop otherwise.
 template <int RW>
 static cudaError_t launch_down_v4_rw(const DownArgs& a, size_t smem, int dev, int sm_count, cudaStream_t st,
                                      bool pdl) {
-    switch (dn4_cl(a.s, RW, sm_count)) {
-        case 1: return launch_down_v4_k<RW, 1>(a, smem, dev, st, pdl);
-        case 2: return launch_down_v4_k<RW, 2>(a, smem, dev, st, pdl);
-        default: return launch_down_v4_k<RW, 4>(a, smem, dev, st, pdl);
+    const int nch = a.s.I / 256;
+    if constexpr (RW == 2) {
+        if (nch == 3) return launch_down_v4_cl<RW, 3>(a, smem, dev, sm_count, st, pdl);
     }
+    if constexpr (RW == 1) {
+        if (nch == 8) return launch_down_v4_cl<RW, 8>(a, smem, dev, sm_count, st, pdl);
+    }
+    return launch_down_v4_cl<RW, 0>(a, smem, dev, sm_count, st, pdl);
 }
 
 // ---- down v5 plan: slab, stage layout, ring depth, row block and cluster
@@ -2780,7 +2800,7 @@ static bool down_v5_plan(const DownArgs& a, const DeviceInfo& di, int dev, DN5Pl
     const DecodeShape& s = a.s;
     if (s.B > MOEDEC_DN5_MAXB || s.I % 256 || s.d % 2) return false;
     DN5Params P{};
-    if (s.I <= 768) {
+    if (s.I == 256 || s.I == 512 || s.I == 768) {
         P.KSLAB = s.I;
         P.scale2d = 0;
     } else if (s.I % 512 == 0) {
@@ -2847,14 +2867,14 @@ static bool down_v5_maps(const DownArgs& a, const DN5Params& P, DN5Maps* maps) {
     for (int sh = 0; sh < 2; ++sh) {
         const MXView& m = sh && !s.S ? v[0] : v[sh];  // no shared expert: any valid map
         const uint64_t rows = (uint64_t)(sh && s.S ? 1 : s.E) * s.d;
-        if (!map_2d_u8(&maps->w[sh], m.w, rows, s.I, P.RT, 128, true)) return false;
+        if (!map_3d_u8_blocks(&maps->w[sh], m.w, rows, s.I, P.RT, P.KSLAB / 128)) return false;
         if (P.scale2d && !map_2d_u8(&maps->s[sh], m.s, rows, s.I / 32, P.RT, 16)) return false;
         if (!P.scale2d) maps->s[sh] = maps->w[sh];  // unused
     }
     return true;
 }
 
-template <int CL>
+template <int CL, int KSLAB>
 static cudaError_t launch_down_v5_k(const DownArgs& a, const DN5Maps& maps, const DN5Plan& pl, int dev,
                                     cudaStream_t st, bool pdl) {
     static std::mutex mu;
@@ -2862,7 +2882,7 @@ static cudaError_t launch_down_v5_k(const DownArgs& a, const DN5Maps& maps, cons
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev >= 64 || attr_smem[dev] < pl.smem) {
-            cudaError_t err = cudaFuncSetAttribute(down_v5_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaError_t err = cudaFuncSetAttribute(down_v5_kernel<CL, KSLAB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    (int)std::max<size_t>(pl.smem, 48 * 1024));
             if (err != cudaSuccess) return err;
             if (dev < 64) attr_smem[dev] = pl.smem;
@@ -2889,7 +2909,7 @@ static cudaError_t launch_down_v5_k(const DownArgs& a, const DN5Maps& maps, cons
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, down_v5_kernel<CL>, a, maps, pl.P);
+    return cudaLaunchKernelEx(&cfg, down_v5_kernel<CL, KSLAB>, a, maps, pl.P);
 }
 
 cudaError_t launch_down(const DecodeShape& s, const void* h, const int32_t* ids, const float* w,
@@ -2905,8 +2925,15 @@ cudaError_t launch_down(const DecodeShape& s, const void* h, const int32_t* ids,
         DN5Plan pl;
         DN5Maps maps;
         if (down_v5_plan(a, di, dev, &pl) && down_v5_maps(a, pl.P, &maps)) {
-            if (pl.CL > 1) return launch_down_v5_k<2>(a, maps, pl, dev, st, after_gate_up);
-            return launch_down_v5_k<1>(a, maps, pl, dev, st, after_gate_up);
+            const int ks = pl.P.KSLAB;
+            if (pl.CL > 1) {
+                if (ks == 768) return launch_down_v5_k<2, 768>(a, maps, pl, dev, st, after_gate_up);
+                if (ks == 512) return launch_down_v5_k<2, 512>(a, maps, pl, dev, st, after_gate_up);
+                return launch_down_v5_k<2, 256>(a, maps, pl, dev, st, after_gate_up);
+            }
+            if (ks == 768) return launch_down_v5_k<1, 768>(a, maps, pl, dev, st, after_gate_up);
+            if (ks == 512) return launch_down_v5_k<1, 512>(a, maps, pl, dev, st, after_gate_up);
+            return launch_down_v5_k<1, 256>(a, maps, pl, dev, st, after_gate_up);
         }
     }
 #endif
