@@ -1735,13 +1735,10 @@ __global__ void __launch_bounds__(DN3_THREADS, 2) down_v3_kernel(DownArgs a) {
 // RT / CL of the rows.  Larger blocks mean bigger bulk copies and fewer h
 // reads; the cluster split keeps enough CTAs.
 
-constexpr int DN4_CW = 8;
-constexpr int DN4_THREADS = (DN4_CW + 1) * 32;
 constexpr int DN4_SMAX = 8;
 constexpr int DN4_RING_BYTES = 96 * 1024;  // two CTAs per SM
 
-__host__ __device__ inline DN3Layout dn4_layout(const DecodeShape& s, int RW) {
-    const int RT = DN4_CW * RW;
+__host__ __device__ inline DN3Layout dn4_layout(const DecodeShape& s, int RT) {
     DN3Layout L;
     L.w_off = 0;
     L.s_off = RT * s.I;
@@ -1752,8 +1749,8 @@ __host__ __device__ inline DN3Layout dn4_layout(const DecodeShape& s, int RW) {
     return L;
 }
 
-__host__ __device__ inline size_t dn4_smem_offset(const DecodeShape& s, int RW) {
-    const size_t acc = (size_t)DN4_CW * RW * s.B * 4;
+__host__ __device__ inline size_t dn4_smem_offset(const DecodeShape& s, int RT) {
+    const size_t acc = (size_t)RT * s.B * 4;
     return (map_ints(s, true) * 4 + acc + 127) / 128 * 128;
 }
 
@@ -1776,22 +1773,22 @@ __device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t ran
     return v;
 }
 
-template <int RW, int CL, int NCH>
-__global__ void __launch_bounds__(DN4_THREADS, 2) down_v4_kernel(DownArgs a) {
-    constexpr int RT = DN4_CW * RW;
+template <int RW, int CL, int NCH, int CW>
+__global__ void __launch_bounds__((CW + 1) * 32, 2) down_v4_kernel(DownArgs a) {
+    constexpr int RT = CW * RW;
     extern __shared__ __align__(128) int smem_i[];
     const DecodeShape s = a.s;
     const RouteMap m = carve_map(smem_i, s, true);
     float* acc = reinterpret_cast<float*>(smem_i + map_ints(s, true));  // [RT][B]
-    const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_i) + dn4_smem_offset(s, RW);
+    const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_i) + dn4_smem_offset(s, RT);
     char* ring = reinterpret_cast<char*>((raw + 127) & ~uintptr_t(127));
-    const DN3Layout L = dn4_layout(s, RW);
+    const DN3Layout L = dn4_layout(s, RT);
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)L.S * L.stage_bytes);
     uint64_t* empty = full + DN4_SMAX;
     if (threadIdx.x == 0) {
         for (int i = 0; i < L.S; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], DN4_CW);
+            mbar_init(&empty[i], CW);
         }
         mbar_init_fence();
     }
@@ -1800,14 +1797,15 @@ __global__ void __launch_bounds__(DN4_THREADS, 2) down_v4_kernel(DownArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = CL > 1 ? (int)cluster_rank() : 0;
     const int o0 = (blockIdx.x / CL) * RT;
+    const int rows = min(RT, s.d - o0);  // the last block may be partial (rows is even)
     const int nu = m.hdr[0];
     bool ok = true;
 
-    if (warp == DN4_CW) {
+    if (warp == CW) {
         // ---------------- producer ----------------
         const uint64_t pol = l2_evict_first_policy();
         const int nb = s.I / 32;
-        const uint32_t wbytes = RT * s.I, sbytes = RT * nb;
+        const uint32_t wbytes = rows * s.I, sbytes = rows * nb;
         auto issue_w = [&](int u, int t0, int slot) {
             const int nt = min(TC, m.ucnt[u] - t0);
             const int e = m.uexp[u];
@@ -1910,7 +1908,7 @@ __global__ void __launch_bounds__(DN4_THREADS, 2) down_v4_kernel(DownArgs a) {
         float sum = 0.f;
 #pragma unroll
         for (int q = 0; q < CL; ++q) sum += CL > 1 ? ld_cluster_f32(p, q) : *p;
-        a.y[(size_t)b * s.d + o0 + rl] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+        if (rl < rows) a.y[(size_t)b * s.d + o0 + rl] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
     }
     if (CL > 1) cluster_sync_all();  // keep this CTA's accumulators alive for its peers
     if (!ok && lane == 0) atomicOr(a.err, MOE_DEVERR_TIMEOUT);
@@ -2692,30 +2690,30 @@ static cudaError_t launch_down_v3(const DownArgs& a, size_t smem, int dev, cudaS
 #endif
 static int dn4_rw(int I) { return I >= 2048 ? 1 : (I >= 1024 ? 2 : MOEDEC_DN4_RWSMALL); }
 
-static size_t down_v4_smem(const DecodeShape& s, int RW) {
-    const DN3Layout L = dn4_layout(s, RW);
+static size_t down_v4_smem(const DecodeShape& s, int RT) {
+    const DN3Layout L = dn4_layout(s, RT);
     if (L.S < 2) return ~(size_t)0;
-    return dn4_smem_offset(s, RW) + (size_t)L.S * L.stage_bytes + 2 * DN4_SMAX * sizeof(uint64_t) + 128;
+    return dn4_smem_offset(s, RT) + (size_t)L.S * L.stage_bytes + 2 * DN4_SMAX * sizeof(uint64_t) + 128;
 }
 
-template <int RW, int CL, int NCH>
+template <int RW, int CL, int NCH, int CW>
 static cudaError_t launch_down_v4_k(const DownArgs& a, size_t smem, int dev, cudaStream_t st, bool pdl) {
     static std::mutex mu;
     static size_t attr_smem[64] = {0};
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev >= 64 || attr_smem[dev] < smem) {
-            cudaError_t err = cudaFuncSetAttribute(down_v4_kernel<RW, CL, NCH>,
+            cudaError_t err = cudaFuncSetAttribute(down_v4_kernel<RW, CL, NCH, CW>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    (int)std::max<size_t>(smem, 48 * 1024));
             if (err != cudaSuccess) return err;
             if (dev < 64) attr_smem[dev] = smem;
         }
     }
-    constexpr int RT = DN4_CW * RW;
+    constexpr int RT = CW * RW;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(a.s.d / RT * CL));
-    cfg.blockDim = dim3(DN4_THREADS);
+    cfg.gridDim = dim3((unsigned)((a.s.d + RT - 1) / RT * CL));
+    cfg.blockDim = dim3((CW + 1) * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
@@ -2734,41 +2732,75 @@ static cudaError_t launch_down_v4_k(const DownArgs& a, size_t smem, int dev, cud
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, down_v4_kernel<RW, CL, NCH>, a);
+    return cudaLaunchKernelEx(&cfg, down_v4_kernel<RW, CL, NCH, CW>, a);
 }
 
-// Cluster size: enough CTAs to fill the GPU twice, never more than the
-// distinct experts a call can have.
-static int dn4_cl(const DecodeShape& s, int RW, int sm_count) {
-    const int blocks = s.d / (DN4_CW * RW);
-    int cl = 1;
-    while (cl < 4 && blocks * cl < 2 * sm_count * 3 / 4 && cl * 2 <= max_unique(s)) cl *= 2;
-    return cl;
+// Consumer warps per CTA (8, or 7 = 14-row blocks with two rows per warp)
+// and cluster size: the fewest rows per CTA over the waves the grid needs at
+// two CTAs per SM, never a cluster larger than the distinct experts a call
+// can have; ties go to 8 warps, then to the smaller cluster.
+struct DN4Geom {
+    int cw, cl;
+};
+
+#ifndef MOEDEC_DN4_CW7
+#define MOEDEC_DN4_CW7 1
+#endif
+
+static DN4Geom dn4_geom(const DecodeShape& s, int RW, int sm_count) {
+    const long slots = 2L * sm_count;
+    DN4Geom best{8, 1};
+    long best_cost = -1;
+    for (int cw = 8; cw >= 7; --cw) {
+        if (cw == 7 && (RW != 2 || !MOEDEC_DN4_CW7)) continue;
+        const int RT = cw * RW;
+        const long nblk = (s.d + RT - 1) / RT;
+        for (int cl = 1; cl <= (cw == 8 ? 4 : 2); cl *= 2) {
+            if (cl > 1 && cl > max_unique(s)) break;
+            const long waves = (nblk * cl + slots - 1) / slots;
+            const long cost = waves * RT * 64 / cl;
+            if (best_cost < 0 || cost < best_cost) {
+                best_cost = cost;
+                best = DN4Geom{cw, cl};
+            }
+        }
+    }
+    return best;
+}
+
+template <int RW, int NCH, int CW>
+static cudaError_t launch_down_v4_cl(const DownArgs& a, int cl, size_t smem, int dev, cudaStream_t st, bool pdl) {
+    switch (cl) {
+        case 1: return launch_down_v4_k<RW, 1, NCH, CW>(a, smem, dev, st, pdl);
+        case 2: return launch_down_v4_k<RW, 2, NCH, CW>(a, smem, dev, st, pdl);
+        default:
+            if constexpr (CW == 8) return launch_down_v4_k<RW, 4, NCH, CW>(a, smem, dev, st, pdl);
+            return cudaErrorInvalidValue;
+    }
 }
 
 template <int RW, int NCH>
-static cudaError_t launch_down_v4_cl(const DownArgs& a, size_t smem, int dev, int sm_count, cudaStream_t st,
+static cudaError_t launch_down_v4_cw(const DownArgs& a, const DN4Geom& g, size_t smem, int dev, cudaStream_t st,
                                      bool pdl) {
-    switch (dn4_cl(a.s, RW, sm_count)) {
-        case 1: return launch_down_v4_k<RW, 1, NCH>(a, smem, dev, st, pdl);
-        case 2: return launch_down_v4_k<RW, 2, NCH>(a, smem, dev, st, pdl);
-        default: return launch_down_v4_k<RW, 4, NCH>(a, smem, dev, st, pdl);
+    if constexpr (RW == 2) {
+        if (g.cw == 7) return launch_down_v4_cl<RW, NCH, 7>(a, g.cl, smem, dev, st, pdl);
     }
+    return launch_down_v4_cl<RW, NCH, 8>(a, g.cl, smem, dev, st, pdl);
 }
 
 // The chunk loop is unrolled for the common lengths (I = 768 at two rows per
 // warp, I = 2048 at one), a run-time loop otherwise.
 template <int RW>
-static cudaError_t launch_down_v4_rw(const DownArgs& a, size_t smem, int dev, int sm_count, cudaStream_t st,
+static cudaError_t launch_down_v4_rw(const DownArgs& a, const DN4Geom& g, size_t smem, int dev, cudaStream_t st,
                                      bool pdl) {
     const int nch = a.s.I / 256;
     if constexpr (RW == 2) {
-        if (nch == 3) return launch_down_v4_cl<RW, 3>(a, smem, dev, sm_count, st, pdl);
+        if (nch == 3) return launch_down_v4_cw<RW, 3>(a, g, smem, dev, st, pdl);
     }
     if constexpr (RW == 1) {
-        if (nch == 8) return launch_down_v4_cl<RW, 8>(a, smem, dev, sm_count, st, pdl);
+        if (nch == 8) return launch_down_v4_cw<RW, 8>(a, g, smem, dev, st, pdl);
     }
-    return launch_down_v4_cl<RW, 0>(a, smem, dev, sm_count, st, pdl);
+    return launch_down_v4_cw<RW, 0>(a, g, smem, dev, st, pdl);
 }
 
 // ---- down v5 plan: slab, stage layout, ring depth, row block and cluster
@@ -2939,15 +2971,15 @@ cudaError_t launch_down(const DecodeShape& s, const void* h, const int32_t* ids,
 #endif
 #ifndef MOEDEC_NO_DN4
     if (down_v3_ok(s, wd, shd)) {
+        // rows per block and s.d even: every block's scale bytes are a multiple of 16
         const int RW = dn4_rw(s.I);
-        if (s.d % (DN4_CW * RW) == 0) {
-            const size_t smem4 = down_v4_smem(s, RW);
-            if (smem4 <= (size_t)di.max_smem_optin) {
-                switch (RW) {
-                    case 1: return launch_down_v4_rw<1>(a, smem4, dev, di.sm_count, st, after_gate_up);
-                    case 2: return launch_down_v4_rw<2>(a, smem4, dev, di.sm_count, st, after_gate_up);
-                    default: return launch_down_v4_rw<4>(a, smem4, dev, di.sm_count, st, after_gate_up);
-                }
+        const DN4Geom g = dn4_geom(s, RW, di.sm_count);
+        const size_t smem4 = down_v4_smem(s, g.cw * RW);
+        if (s.d % 2 == 0 && smem4 <= (size_t)di.max_smem_optin) {
+            switch (RW) {
+                case 1: return launch_down_v4_rw<1>(a, g, smem4, dev, st, after_gate_up);
+                case 2: return launch_down_v4_rw<2>(a, g, smem4, dev, st, after_gate_up);
+                default: return launch_down_v4_rw<4>(a, g, smem4, dev, st, after_gate_up);
             }
         }
     }

@@ -87,6 +87,50 @@ def test_edge_shapes(cuda_device, E, k, d, I, shared):
         compare_tokens(cuda_device, W, Wd, x, ids, w, range(B), f"edge {E},{k},{d},{I},{shared} B={B}")
 
 
+def _layer_with_canaries(dev, Wd, x, ids, w, shared):
+    """Run moe_layer with y and the workspace cut out of larger buffers whose
+    guard bytes hold a fixed pattern; returns y and whether every guard byte
+    is still intact."""
+    B, d = x.shape
+    k = ids.shape[1]
+    I = Wd["gate"].w.shape[1]
+    G = 512  # guard bytes on each side (keeps both regions 512-byte aligned)
+    need = moe.layer_workspace_bytes(B, k, I, shared)
+    ws_buf = torch.full((need + 2 * G,), 0xA5, dtype=torch.uint8, device=dev)
+    y_buf = torch.full((2 * B * d + 2 * G,), 0x5A, dtype=torch.uint8, device=dev)
+    y = y_buf[G:G + 2 * B * d].view(torch.bfloat16).view(B, d)
+    moe.layer(x.to(dev), ids.to(dev), w.to(dev), Wd["gate"], Wd["up"], Wd["down"], shared=Wd["shared"],
+              workspace=ws_buf[G:G + need], y=y)
+    torch.cuda.synchronize()
+    intact = bool((ws_buf[:G] == 0xA5).all() and (ws_buf[G + need:] == 0xA5).all()
+                  and (y_buf[:G] == 0x5A).all() and (y_buf[G + 2 * B * d:] == 0x5A).all())
+    return y, intact
+
+
+@pytest.mark.parametrize("B", [1, 3])
+def test_outputs_stay_in_bounds_qwen(cuda_device, qwen, B):
+    """The layer writes y [B][d] and h at the head of the workspace and no
+    byte around them (the down pass's row blocks need not divide d)."""
+    W, Wd = qwen
+    x, ids, w = inputs.layer_batch(inputs.QWEN3, B)
+    y, intact = _layer_with_canaries(cuda_device, Wd, x, ids, w, False)
+    assert intact, "a kernel wrote outside y or the workspace"
+    assert torch.isfinite(y.float()).all()
+    compare_tokens(cuda_device, W, Wd, x, ids, w, range(B), f"qwen canary B={B}")
+
+
+@pytest.mark.parametrize("E,k,d,I,shared", [(2, 2, 1024, 512, False), (5, 2, 1536, 768, True)])
+def test_outputs_stay_in_bounds_edge(cuda_device, E, k, d, I, shared):
+    W = small_weights(E, d, I, shared, 3)
+    Wd = device_mx(W, cuda_device)
+    for B in (1, 4):
+        cfg = inputs.LayerConfig("canary", E, k, d, I, shared, "softmax_normal")
+        x, ids, w = inputs.layer_batch(cfg, B, step=E * 10 + d)
+        y, intact = _layer_with_canaries(cuda_device, Wd, x, ids, w, shared)
+        assert intact, f"a kernel wrote outside y or the workspace ({E},{k},{d},{I},{shared}) B={B}"
+        compare_tokens(cuda_device, W, Wd, x, ids, w, range(B), f"canary {E},{k},{d},{I},{shared} B={B}")
+
+
 def test_hot_expert_and_duplicates(cuda_device):
     """Every token on one expert (more tokens than one pass serves) and the
     same expert twice inside one token's top-k (summed independently)."""
