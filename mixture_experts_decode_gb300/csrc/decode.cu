@@ -113,29 +113,68 @@ __device__ RouteMap carve_map(int* p, const DecodeShape& s, bool with_w) {
 
 __device__ void build_route_map(const RouteMap& m, const int32_t* __restrict__ ids,
                                 const float* __restrict__ w, const DecodeShape& s, int* err,
-                                bool merge = false) {
+                                bool merge = false, int* scratch = nullptr, int scratch_ints = 0) {
     // The first PT = min(blockDim.x, DEC_THREADS) threads (whole warps) build
     // the map; any further threads only take part in the barriers.
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int PT = min((int)blockDim.x, DEC_THREADS) & ~31, PW = PT >> 5;
     const bool part = tid < PT;
     const int n = s.B * s.k;
-    if (part)
-        for (int e = tid; e < s.E; e += PT) m.cnt[e] = 0;
-    __syncthreads();
-    if (part) {
-        int bad = 0;
-        for (int f = tid; f < n; f += PT) {
-            int e = ids[f];
-            if ((unsigned)e < (unsigned)s.E) {
-                atomicAdd(&m.cnt[e], 1);
-            } else {
-                e = -1;
-                bad = 1;
-            }
-            m.sid[f] = e;
+    // Parallel placement (32 < n <= PT, with a PW x E scratch table, e.g. the
+    // idle copy ring; one warp's worth of slots is placed as fast serially):
+    // thread f holds slot f; its position inside its expert's
+    // range is the number of earlier slots with the same expert, i.e. the
+    // slots of earlier warps (per-warp counts, scanned over warps) plus the
+    // earlier lanes of its own warp (a match mask).
+    const bool fast = n > 32 && n <= PT && scratch != nullptr && scratch_ints >= s.E * PW;
+    int my_e = -1, my_rank = 0;
+    float my_w = 0.f;
+    if (fast) {
+        if (tid < n) {
+            my_e = ids[tid];
+            if (w) my_w = w[tid];
         }
-        if (bad) atomicOr(err, MOE_DEVERR_EXPERT_ID);
+        for (int i = tid; i < s.E * PW; i += blockDim.x) scratch[i] = 0;
+        if (tid < n && (unsigned)my_e >= (unsigned)s.E) {
+            my_e = -1;
+            atomicOr(err, MOE_DEVERR_EXPERT_ID);
+        }
+        __syncthreads();
+        if (part) {
+            const unsigned mask = __match_any_sync(FULL_MASK, my_e);
+            my_rank = __popc(mask & lanemask_lt());
+            if (my_e >= 0 && my_rank == 0) scratch[my_e * PW + warp] = __popc(mask);
+        }
+        __syncthreads();
+        // per expert: counts of the earlier warps (exclusive) and the total
+        if (part)
+            for (int e = tid; e < s.E; e += PT) {
+                int c = 0;
+                for (int q = 0; q < PW; ++q) {
+                    const int t = scratch[e * PW + q];
+                    scratch[e * PW + q] = c;
+                    c += t;
+                }
+                m.cnt[e] = c;
+            }
+    } else {
+        if (part)
+            for (int e = tid; e < s.E; e += PT) m.cnt[e] = 0;
+        __syncthreads();
+        if (part) {
+            int bad = 0;
+            for (int f = tid; f < n; f += PT) {
+                int e = ids[f];
+                if ((unsigned)e < (unsigned)s.E) {
+                    atomicAdd(&m.cnt[e], 1);
+                } else {
+                    e = -1;
+                    bad = 1;
+                }
+                m.sid[f] = e;
+            }
+            if (bad) atomicOr(err, MOE_DEVERR_EXPERT_ID);
+        }
     }
     __syncthreads();
 
@@ -186,11 +225,18 @@ __device__ void build_route_map(const RouteMap& m, const int32_t* __restrict__ i
     }
     __syncthreads();
 
-    // Stable placement of slots into their expert's range (one warp; the
-    // order inside an expert is increasing flat slot index).
+    // Stable placement of slots into their expert's range (the order inside
+    // an expert is increasing flat slot index).
     const int nu = m.hdr[1], tot = m.hdr[2];
     const int KS = s.k + s.S;
-    if (warp == 0) {
+    if (fast) {
+        if (my_e >= 0) {
+            const int pos = m.cnt[my_e] + scratch[my_e * PW + warp] + my_rank;
+            const int b = tid / s.k, j = tid - b * s.k;
+            m.hrow[pos] = b * KS + j;
+            if (m.wt) m.wt[pos] = my_w;
+        }
+    } else if (warp == 0) {
         for (int f0 = 0; f0 < n; f0 += 32) {
             const int f = f0 + lane;
             const int e = f < n ? m.sid[f] : -1;
@@ -872,7 +918,9 @@ __global__ void __launch_bounds__(GU3_THREADS, MOEDEC_GU3_MINB)
         }
         mbar_init_fence();
     }
-    build_route_map(m, a.ids, nullptr, s, a.err);  // ends with __syncthreads
+    // the copy ring is idle until the map is built: it serves as the map's scratch
+    build_route_map(m, a.ids, nullptr, s, a.err, false, reinterpret_cast<int*>(sm->st),
+                    (int)(sizeof(sm->st) / 4));  // ends with __syncthreads
     asm volatile("griddepcontrol.launch_dependents;");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1164,7 +1212,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, RT == 32 ? 1 : 2)
         sh->abort = 0;
         mbar_init_fence();
     }
-    build_route_map(m, a.ids, nullptr, s, a.err);  // ends with __syncthreads
+    // the copy ring is idle until the map is built: it serves as the map's scratch
+    build_route_map(m, a.ids, nullptr, s, a.err, false, reinterpret_cast<int*>(ring),
+                    (int)(S * sizeof(GU4Stage<RT>) / 4));  // ends with __syncthreads
     asm volatile("griddepcontrol.launch_dependents;");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1792,7 +1842,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, 2) down_v4_kernel(DownArgs a) {
         }
         mbar_init_fence();
     }
-    build_route_map(m, a.ids, a.w, s, a.err, true);  // ends with __syncthreads
+    // the copy ring is idle until the map is built: it serves as the map's scratch
+    build_route_map(m, a.ids, a.w, s, a.err, true, reinterpret_cast<int*>(ring),
+                    L.S * L.stage_bytes / 4);  // ends with __syncthreads
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = CL > 1 ? (int)cluster_rank() : 0;
@@ -2048,7 +2100,9 @@ __global__ void __launch_bounds__(DN5_THREADS, 2)
         *abortf = 0;
         mbar_init_fence();
     }
-    build_route_map(m, a.ids, a.w, s, a.err, true);  // ends with __syncthreads
+    // the copy ring is idle until the map is built: it serves as the map's scratch
+    build_route_map(m, a.ids, a.w, s, a.err, true, reinterpret_cast<int*>(ring),
+                    S * P.stage_bytes / 4);  // ends with __syncthreads
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = CL > 1 ? (int)cluster_rank() : 0;
@@ -2752,11 +2806,13 @@ static DN4Geom dn4_geom(const DecodeShape& s, int RW, int sm_count) {
     DN4Geom best{8, 1};
     long best_cost = -1;
     for (int cw = 8; cw >= 7; --cw) {
-        if (cw == 7 && (RW != 2 || !MOEDEC_DN4_CW7)) continue;
+        if (cw == 7 && (RW == 1 || !MOEDEC_DN4_CW7)) continue;
+        if (cw == 8 && RW == 4 && MOEDEC_DN4_CW7) continue;  // four rows per warp want the 128-register CTA
         const int RT = cw * RW;
         const long nblk = (s.d + RT - 1) / RT;
-        for (int cl = 1; cl <= (cw == 8 ? 4 : 2); cl *= 2) {
+        for (int cl = 1; cl <= 4; cl *= 2) {
             if (cl > 1 && cl > max_unique(s)) break;
+            if (RT % cl) continue;
             const long waves = (nblk * cl + slots - 1) / slots;
             const long cost = waves * RT * 64 / cl;
             if (best_cost < 0 || cost < best_cost) {
@@ -2774,7 +2830,7 @@ static cudaError_t launch_down_v4_cl(const DownArgs& a, int cl, size_t smem, int
         case 1: return launch_down_v4_k<RW, 1, NCH, CW>(a, smem, dev, st, pdl);
         case 2: return launch_down_v4_k<RW, 2, NCH, CW>(a, smem, dev, st, pdl);
         default:
-            if constexpr (CW == 8) return launch_down_v4_k<RW, 4, NCH, CW>(a, smem, dev, st, pdl);
+            if constexpr ((CW * RW) % 4 == 0) return launch_down_v4_k<RW, 4, NCH, CW>(a, smem, dev, st, pdl);
             return cudaErrorInvalidValue;
     }
 }
@@ -2782,7 +2838,7 @@ static cudaError_t launch_down_v4_cl(const DownArgs& a, int cl, size_t smem, int
 template <int RW, int NCH>
 static cudaError_t launch_down_v4_cw(const DownArgs& a, const DN4Geom& g, size_t smem, int dev, cudaStream_t st,
                                      bool pdl) {
-    if constexpr (RW == 2) {
+    if constexpr (RW >= 2) {
         if (g.cw == 7) return launch_down_v4_cl<RW, NCH, 7>(a, g.cl, smem, dev, st, pdl);
     }
     return launch_down_v4_cl<RW, NCH, 8>(a, g.cl, smem, dev, st, pdl);
@@ -2794,7 +2850,7 @@ template <int RW>
 static cudaError_t launch_down_v4_rw(const DownArgs& a, const DN4Geom& g, size_t smem, int dev, cudaStream_t st,
                                      bool pdl) {
     const int nch = a.s.I / 256;
-    if constexpr (RW == 2) {
+    if constexpr (RW >= 2) {
         if (nch == 3) return launch_down_v4_cw<RW, 3>(a, g, smem, dev, st, pdl);
     }
     if constexpr (RW == 1) {
