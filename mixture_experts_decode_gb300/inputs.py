@@ -122,6 +122,18 @@ def route(kind: str, B: int, E: int, k: int, *key):
     return ids.to(torch.int32).contiguous(), w.to(torch.float32).contiguous()
 
 
+def router_logits(kind: str, B: int, E: int, *key) -> torch.Tensor:
+    """Router logits float32 [B, E] (CPU) with the distributions of the
+    routings above: U[0, 1) for "softmax_uniform", N(0, 1) for
+    "softmax_normal" and "sigmoid_scaled"."""
+    g = _gen("cpu", *key, "router_logits")
+    if kind == "softmax_uniform":
+        return torch.rand((B, E), generator=g, dtype=torch.float32)
+    if kind in ("softmax_normal", "sigmoid_scaled"):
+        return torch.randn((B, E), generator=g, dtype=torch.float32)
+    raise ValueError(f"no router logits for routing {kind!r}")
+
+
 # ------------------------------------------------------------- workloads ---
 
 @dataclasses.dataclass(frozen=True)

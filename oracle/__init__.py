@@ -37,6 +37,9 @@ def _load():
                                          P, P, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_align_sizes.restype = ctypes.c_int
         lib.oracle_align_sizes.argtypes = [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_int64)] * 2
+        lib.oracle_router_topk.restype = ctypes.c_int
+        lib.oracle_router_topk.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_double, P, P]
         lib.oracle_align.restype = ctypes.c_int
         lib.oracle_align.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      P, ctypes.c_int64, P, ctypes.c_int64, P]
@@ -135,3 +138,17 @@ def align(topk_ids, E: int, block_size: int):
     if rc != 0:
         raise ValueError(f"oracle_align rejected its arguments (rc={rc})")
     return sorted_ids, expert_ids, int(ntpp[0])
+
+
+def router_topk(logits, k: int, score: str = "softmax", scale: float = 1.0):
+    """Routing by definition (see moe_oracle.c): logits float32 [B, E] ->
+    (ids int32 [B, k], w float64 [B, k]); score "softmax" or "sigmoid"."""
+    lg = _c(logits, np.float32)
+    B, E = lg.shape
+    ids = np.empty((B, k), dtype=np.int32)
+    w = np.empty((B, k), dtype=np.float64)
+    rc = _load().oracle_router_topk(_ptr(lg), B, E, k, {"softmax": 0, "sigmoid": 1}[score], float(scale),
+                                    _ptr(ids), _ptr(w))
+    if rc != 0:
+        raise ValueError(f"oracle_router_topk rejected its arguments (rc={rc})")
+    return ids, w

@@ -262,3 +262,58 @@ int oracle_align(const int32_t* ids, int T, int k, int E, int block_size, int32_
     free(cnt); free(start); free(pos);
     return rc;
 }
+
+/* ---------------------------------------------------------- router [AS] --- */
+
+/* The routing step in front of the decode layer ([AS], section
+ * "MoE Align & Sort CUDA算法在其他开源平台的实现": FasterTransformer's fused
+ * topk_gating_softmax), per token b, by definition:
+ *   score 0 (softmax): p = softmax over all E logits; the k largest p (ties:
+ *     lower expert index first), in descending order; w_j = scale * p_j /
+ *     (sum of the k chosen p);
+ *   score 1 (sigmoid): s = 1 / (1 + exp(-logit)) for all E; the k largest s,
+ *     same order; w_j = scale * s_j / (sum of the k chosen s).
+ * Selection is k passes of "largest remaining score, lowest index on ties";
+ * scores are FP64 from the FP32 logits. */
+int oracle_router_topk(const float* logits, int B, int E, int k, int score, double scale, int32_t* ids,
+                       double* w) {
+    if (B < 0 || E < 1 || k < 1 || k > E || (score != 0 && score != 1)) return ORACLE_ERR_ARG;
+    double* sc = (double*)malloc(sizeof(double) * (size_t)E);
+    char* used = (char*)malloc((size_t)E);
+    if (!sc || !used) {
+        free(sc);
+        free(used);
+        return ORACLE_ERR_ARG;
+    }
+    for (int b = 0; b < B; ++b) {
+        const float* l = logits + (size_t)b * E;
+        if (score == 0) {
+            double m = l[0];
+            for (int e = 1; e < E; ++e)
+                if (l[e] > m) m = l[e];
+            double z = 0.0;
+            for (int e = 0; e < E; ++e) {
+                sc[e] = exp((double)l[e] - m);
+                z += sc[e];
+            }
+            for (int e = 0; e < E; ++e) sc[e] /= z;
+        } else {
+            for (int e = 0; e < E; ++e) sc[e] = 1.0 / (1.0 + exp(-(double)l[e]));
+        }
+        memset(used, 0, (size_t)E);
+        double tot = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e)
+                if (!used[e] && (best < 0 || sc[e] > sc[best])) best = e;
+            used[best] = 1;
+            ids[(size_t)b * k + j] = best;
+            w[(size_t)b * k + j] = sc[best];
+            tot += sc[best];
+        }
+        for (int j = 0; j < k; ++j) w[(size_t)b * k + j] = scale * w[(size_t)b * k + j] / tot;
+    }
+    free(sc);
+    free(used);
+    return ORACLE_OK;
+}
