@@ -273,8 +273,10 @@ int oracle_align(const int32_t* ids, int T, int k, int E, int block_size, int32_
  *     (sum of the k chosen p);
  *   score 1 (sigmoid): s = 1 / (1 + exp(-logit)) for all E; the k largest s,
  *     same order; w_j = scale * s_j / (sum of the k chosen s).
- * Selection is k passes of "largest remaining score, lowest index on ties";
- * scores are FP64 from the FP32 logits. */
+ * Selection is k passes of "largest remaining, lowest index on ties", taken
+ * on the FP32 logits themselves: both score maps are strictly increasing, so
+ * this is the exact score order (FP64 sigmoid scores can tie where the exact
+ * ones do not, e.g. all logits above ~37 round to 1.0).  Weights are FP64. */
 int oracle_router_topk(const float* logits, int B, int E, int k, int score, double scale, int32_t* ids,
                        double* w) {
     if (B < 0 || E < 1 || k < 1 || k > E || (score != 0 && score != 1)) return ORACLE_ERR_ARG;
@@ -305,7 +307,7 @@ int oracle_router_topk(const float* logits, int B, int E, int k, int score, doub
         for (int j = 0; j < k; ++j) {
             int best = -1;
             for (int e = 0; e < E; ++e)
-                if (!used[e] && (best < 0 || sc[e] > sc[best])) best = e;
+                if (!used[e] && (best < 0 || l[e] > l[best])) best = e;
             used[best] = 1;
             ids[(size_t)b * k + j] = best;
             w[(size_t)b * k + j] = sc[best];

@@ -89,3 +89,11 @@ def test_softmax_shift_invariance_sigmoid_not():
 def test_rejects_bad_arguments():
     with pytest.raises(ValueError):
         oracle.router_topk(np.zeros((2, 4), np.float32), 5)
+
+
+def test_selection_follows_the_logits_where_fp64_scores_saturate():
+    # sigmoid(40) and sigmoid(41) are both 1.0 in FP64; the exact order (41 first) is kept
+    lg = np.array([[40.0, 41.0, -3.0, 0.0]], np.float32)
+    ids, w = oracle.router_topk(lg, 2, "sigmoid", 2.5)
+    assert ids.tolist() == [[1, 0]]
+    np.testing.assert_allclose(w, [[1.25, 1.25]], rtol=1e-12)
