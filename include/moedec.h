@@ -58,6 +58,7 @@ enum moe_status {
 /* Device error bits reported by moe_device_error(). */
 #define MOE_DEVERR_EXPERT_ID 0x1 /* an expert id outside [0, E) was skipped */
 #define MOE_DEVERR_TIMEOUT 0x2   /* a kernel's bounded wait gave up (never expected) */
+#define MOE_DEVERR_LOGIT 0x4     /* a router row had fewer than k logits above -inf */
 
 /* Limits of the decode kernels (moe_gate_up, moe_down, moe_layer*). */
 #define MOE_MAX_EXPERTS 1024  /* E */
@@ -65,6 +66,11 @@ enum moe_status {
 #define MOE_MAX_SLOTS 2048    /* B * k */
 /* Limits of moe_align_block_size. */
 #define MOE_ALIGN_MAX_EXPERTS 1024
+/* Limits and score kinds of moe_router_topk. */
+#define MOE_ROUTER_MAX_EXPERTS 1024
+#define MOE_ROUTER_MAX_K 32
+#define MOE_ROUTER_SOFTMAX 0
+#define MOE_ROUTER_SIGMOID 1
 
 /* One MXFP8 weight tensor: codes [E][rows][K] and scales [E][rows][K/32].
  * Both device pointers; `w` must be 32-byte aligned (K % 32 == 0 then keeps
@@ -224,6 +230,30 @@ int moe_align_static_fits(int T, int k, int E);
  * aligned; bytes a multiple of 32.
  */
 int moe_copy(void* dst, const void* src, size_t bytes, moe_stream_t stream);
+
+/*
+ * moe_router_topk -- the routing step in front of the decode layer: for each
+ * token b, the k largest of its E router logits, in descending order (ties:
+ * the lower expert index first), with their routing weights [AS, section
+ * "MoE Align & Sort CUDA算法在其他开源平台的实现": FasterTransformer's fused
+ * topk_gating_softmax].
+ *   score MOE_ROUTER_SOFTMAX: w_j = scale * p_j / (sum of the k chosen p),
+ *     p = softmax over all E logits (renormalised top-k; scale 1 for the
+ *     plain renormalisation);
+ *   score MOE_ROUTER_SIGMOID: w_j = scale * s_j / (sum of the k chosen s),
+ *     s = 1 / (1 + exp(-logit)) (e.g. scale 2.5 for the DeepSeek-V3 gate).
+ * Both score maps are increasing, so the choice is the k largest logits.
+ *   logits    float32 [B][E], row-major; finite values expected.  A row with
+ *             fewer than k logits above -inf (NaN counts as absent) gets id
+ *             -1 and weight 0 in the missing places and sets
+ *             MOE_DEVERR_LOGIT.
+ *   topk_ids  int32 [B][k] out; topk_w float32 [B][k] out.  4-byte aligned.
+ * Limits: 1 <= E <= MOE_ROUTER_MAX_EXPERTS, 1 <= k <= min(E, MOE_ROUTER_MAX_K),
+ * B >= 0 (B = 0 launches nothing).  Weights are FP32 (expf), within a few
+ * ulps of the exact values.
+ */
+int moe_router_topk(const float* logits, int B, int E, int k, int score, float scale, int32_t* topk_ids,
+                    float* topk_w, moe_stream_t stream);
 
 /*
  * moe_device_error -- synchronise `stream`, then read and clear the sticky

@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "MOE_OK", -1: "MOE_ERR_ARG", -2: "MOE_ERR_SHAPE", -3: "MOE_ER
 EXPORTS = ("moe_version", "moe_strerror", "moe_gate_up", "moe_down", "moe_layer_workspace_bytes",
            "moe_layer", "moe_layer_host_workspace_bytes", "moe_layer_host", "moe_align_sizes",
            "moe_align_block_size", "moe_align_block_size_static", "moe_align_static_fits",
-           "moe_copy", "moe_device_error")
+           "moe_copy", "moe_device_error", "moe_router_topk")
 
 
 class MoEError(RuntimeError):
@@ -69,6 +69,7 @@ def load(path: str = LIB_PATH):
         "moe_align_sizes": ([I, I, I, I, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
                              ctypes.POINTER(S)], I),
         "moe_align_block_size": ([P, I, I, I, I, P, P, P, P, S, P], I),
+        "moe_router_topk": ([P, I, I, I, I, ctypes.c_float, P, P, P], I),
         "moe_align_block_size_static": ([P, I, I, I, I, P, P, P, P], I),
         "moe_align_static_fits": ([I, I, I], I),
         "moe_copy": ([P, P, S, P], I),
@@ -327,3 +328,25 @@ def device_error(device=None) -> int:
     if rc not in (MOE_OK, -7):
         _check("moe_device_error", rc)
     return bits.value
+
+
+ROUTER_SCORES = {"softmax": 0, "sigmoid": 1}
+
+
+def router_topk(logits, k: int, score: str = "softmax", scale: float = 1.0, topk_ids=None, topk_w=None):
+    """moe_router_topk: logits float32 [B, E] (device) -> (topk_ids int32 [B, k],
+    topk_w float32 [B, k]); score "softmax" (renormalised top-k) or "sigmoid"
+    (normalised over the k, times `scale`)."""
+    lib = load()
+    dev = logits.device
+    _need(logits, "logits", torch.float32, None, 2)
+    B, E = logits.shape
+    if topk_ids is None:
+        topk_ids = torch.empty((B, k), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((B, k), dtype=torch.float32, device=dev)
+    _need(topk_ids, "topk_ids", torch.int32, dev)
+    _need(topk_w, "topk_w", torch.float32, dev)
+    _check("moe_router_topk", lib.moe_router_topk(logits.data_ptr(), B, E, k, ROUTER_SCORES[score], float(scale),
+                                                  topk_ids.data_ptr(), topk_w.data_ptr(), _stream(dev)))
+    return topk_ids, topk_w

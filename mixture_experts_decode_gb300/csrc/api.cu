@@ -261,6 +261,18 @@ int moe_layer_host(const void* x_host, int B, int d, const int32_t* topk_ids_hos
     return MOE_OK;
 }
 
+int moe_router_topk(const float* logits, int B, int E, int k, int score, float scale, int32_t* topk_ids,
+                    float* topk_w, moe_stream_t stream) {
+    if (B < 0 || E < 1 || k < 1 || (score != MOE_ROUTER_SOFTMAX && score != MOE_ROUTER_SIGMOID))
+        return MOE_ERR_ARG;
+    if (k > E) return MOE_ERR_SHAPE;
+    if (E > MOE_ROUTER_MAX_EXPERTS || k > MOE_ROUTER_MAX_K) return MOE_ERR_LIMIT;
+    if (B == 0) return MOE_OK;
+    if (!logits || !topk_ids || !topk_w) return MOE_ERR_ARG;
+    if (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_w, 4)) return MOE_ERR_ALIGN;
+    return cuda_status(launch_router(logits, B, E, k, score, scale, topk_ids, topk_w, (cudaStream_t)stream));
+}
+
 int moe_align_sizes(int T, int k, int E, int block_size, int64_t* n_sorted, int64_t* n_blocks,
                     size_t* ws_bytes) {
     if (T < 0 || k < 1 || E < 1 || block_size < 1) return MOE_ERR_ARG;

@@ -28,6 +28,8 @@ cudaError_t launch_gate_up(const DecodeShape& s, const void* x, const int32_t* i
                            MXView wu, MXView shg, MXView shu, void* h, cudaStream_t st);
 cudaError_t launch_down(const DecodeShape& s, const void* h, const int32_t* ids, const float* w,
                         MXView wd, MXView shd, void* y, cudaStream_t st, bool after_gate_up);
+cudaError_t launch_router(const float* logits, int B, int E, int k, int score, float scale, int32_t* ids, float* w,
+                          cudaStream_t st);
 // Shared-memory bytes the decode kernels need; 0 if the shape is beyond the
 // supported limits.
 size_t gate_up_smem_bytes(const DecodeShape& s);

@@ -96,3 +96,16 @@ def test_align_sizes_and_checks(lib):
 def test_host_and_device_workspace_sizes(lib):
     assert moe.layer_host_workspace_bytes(32, 2048, 8, 768, False) >= \
         moe.layer_workspace_bytes(32, 8, 768, False) + 2 * 32 * 2048 * 2
+
+
+def test_router_rejects_bad_arguments_before_launch(lib):
+    P = ctypes.c_void_p
+    good = (P(0x10000), P(0x20000), P(0x30000))
+    assert lib.moe_router_topk(good[0], 4, 8, 9, 0, 1.0, good[1], good[2], None) == -2     # k > E
+    assert lib.moe_router_topk(good[0], 4, 2048, 8, 0, 1.0, good[1], good[2], None) == -3  # E > max
+    assert lib.moe_router_topk(good[0], 4, 64, 33, 0, 1.0, good[1], good[2], None) == -3   # k > max
+    assert lib.moe_router_topk(good[0], 4, 64, 8, 2, 1.0, good[1], good[2], None) == -1    # score
+    assert lib.moe_router_topk(good[0], -1, 64, 8, 0, 1.0, good[1], good[2], None) == -1   # B < 0
+    assert lib.moe_router_topk(None, 4, 64, 8, 0, 1.0, good[1], good[2], None) == -1       # NULL
+    assert lib.moe_router_topk(P(0x10002), 4, 64, 8, 0, 1.0, good[1], good[2], None) == -5  # alignment
+    assert lib.moe_router_topk(None, 0, 64, 8, 1, 2.5, None, None, None) == 0               # B = 0
