@@ -406,6 +406,21 @@ def run_align(dev, stream, ranks, K=200):
             "gbs": nbytes / (secs / K) / 1e9, "algorithmic_bytes": nbytes}
 
 
+def run_router(dev, stream, ranks, cfg, B, K=200):
+    """The routing step for this workload's routing at this batch (one launch)."""
+    import torch
+    import mixture_experts_decode_gb300 as moe
+    from mixture_experts_decode_gb300 import inputs
+    score, scale = ("sigmoid", 2.5) if cfg.routing == "sigmoid_scaled" else ("softmax", 1.0)
+    kind = cfg.routing if cfg.routing in ("softmax_uniform", "softmax_normal", "sigmoid_scaled") else "softmax_normal"
+    lg = inputs.router_logits(kind, B, cfg.E, "bench-router", B).to(dev)
+    ids = torch.empty((B, cfg.k), dtype=torch.int32, device=dev)
+    w = torch.empty((B, cfg.k), dtype=torch.float32, device=dev)
+    secs, _ = time_steps(lambda i: moe.router_topk(lg, cfg.k, score, scale, ids, w), K, 20, stream, ranks, chunk=100)
+    return {"workload": f"router {score} top-{cfg.k} of E={cfg.E}, B={B}" + (f" x{scale}" if score == "sigmoid" else ""),
+            "us": secs / K * 1e6}
+
+
 # -------------------------------------------------------------------- arms ---
 
 def run_ours(args):
@@ -486,6 +501,7 @@ def run_ours(args):
            "api": "moe_layer_host (pinned host x/topk_ids/topk_w -> y)"}
 
     align = run_align(dev, stream, ranks)
+    router = run_router(dev, stream, ranks, cfg, B)
 
     cpu = None
     if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
@@ -508,7 +524,7 @@ def run_ours(args):
         "pct_of_measured_peak": 100 * value * 1e3 / hbm_peak, "pct_of_8tbs_nominal": 100 * value / 8.0,
         "kernels": {"gate_up_us": gu_us, "gate_up_gbs": gu_gbs, "down_us": dn_us, "down_gbs": dn_gbs},
         "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clocks, "align": align,
-        "cpu_baseline": cpu,
+        "router": router, "cpu_baseline": cpu,
     }
     if extra is not None:
         line["sweep"] = extra
