@@ -1018,6 +1018,9 @@ __global__ void __launch_bounds__(GU3_THREADS, MOEDEC_GU3_MINB)
 // barrier.  Two geometries: RT = 32 with 16 consumer warps and one CTA per
 // SM, RT = 16 with 8 consumer warps and two CTAs per SM.
 
+#ifndef MOEDEC_GU4_ORDER
+#define MOEDEC_GU4_ORDER 1
+#endif
 constexpr int GU4_KT = 512;   // K elements per stage (16 scale blocks)
 constexpr int GU4_BOX = 128;  // inner box of a weight tensor copy (bytes)
 constexpr int GU4_S = 4;      // ring stages
@@ -1036,6 +1039,7 @@ struct GU4Shared {
     uint64_t full[GU4_S];
     uint64_t empty[GU4_S];
     int abort;
+    int perm[256];  // distinct experts by descending token count (when at most 256)
 };
 
 struct GU4Maps {
@@ -1192,6 +1196,44 @@ __device__ __forceinline__ void gu4_group(const GateUpArgs& a, GU4Stage<RT>* rin
     }
 }
 
+// The distinct experts u < nu (nu <= 256) ordered by descending slot count,
+// the lower index first on ties, into perm[]: a bitonic sort of packed
+// (255 - count, u) keys by the first 256 threads (shuffles below a distance
+// of 32, `scratch` (256 words) above).  Every thread of the CTA must call it.
+__device__ void order_experts_by_count(const RouteMap& m, int nu, int* perm, uint32_t* scratch) {
+    const int tid = threadIdx.x;
+    const bool part = tid < 256;
+    uint32_t key = 0xffffffffu;
+    if (part && tid < nu) {
+        const int n = m.uoff[tid + 1] - m.uoff[tid];
+        const int c = min(n, 255);
+        key = ((uint32_t)(255 - c) << 16) | (uint32_t)tid;
+    }
+    for (int k = 2; k <= 256; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            uint32_t other = key;
+            if (j >= 32) {
+                if (part) scratch[tid] = key;
+                __syncthreads();
+                if (part) other = scratch[tid ^ j];
+                __syncthreads();
+            } else {
+                other = __shfl_xor_sync(FULL_MASK, key, j);
+            }
+            const bool asc = (tid & k) == 0, low = (tid & j) == 0;
+            if (part) key = low == asc ? min(key, other) : max(key, other);
+        }
+    }
+    if (part && tid < nu) perm[tid] = (int)(key & 0xffffu);
+    __syncthreads();
+}
+
+// Tile of round r for this CTA when tiles are dealt in snake order (round r
+// goes over the CTAs forwards when r is even, backwards when odd).
+__device__ __forceinline__ int snake_tile(int r) {
+    return r * (int)gridDim.x + ((r & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x);
+}
+
 template <int RT, int CW>
 __global__ void __launch_bounds__((CW + 1) * 32, RT == 32 ? 1 : 2)
     gate_up_v4_kernel(GateUpArgs a, const __grid_constant__ GU4Maps maps) {
@@ -1217,10 +1259,19 @@ __global__ void __launch_bounds__((CW + 1) * 32, RT == 32 ? 1 : 2)
                     (int)(S * sizeof(GU4Stage<RT>) / 4));  // ends with __syncthreads
     asm volatile("griddepcontrol.launch_dependents;");
 
+    const int nu = m.hdr[0];
+    const int rbs = s.I / RT;
+    const int tiles = nu * rbs;
+    // With few tiles per CTA and some expert needing more than one pass over
+    // its rows, deal the heaviest experts' tiles first, in snake order over
+    // the CTAs, so that the CTAs' loads even out; otherwise plain round robin.
+    // (The order never changes a result.)
+    bool ordered = (CW + 1) * 32 >= 256 && MOEDEC_GU4_ORDER && nu <= 256 && tiles <= 32 * (int)gridDim.x;
+    if (ordered)  // uniform over the CTA: the map is shared
+        ordered = __syncthreads_or((int)threadIdx.x < nu && m.uoff[threadIdx.x + 1] - m.uoff[threadIdx.x] > TC);
+    if (ordered) order_experts_by_count(m, nu, sh->perm, reinterpret_cast<uint32_t*>(ring));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KS = s.k + s.S;
-    const int rbs = s.I / RT;
-    const int tiles = m.hdr[0] * rbs;
     const int nkt = s.d / GU4_KT;
 
     if (warp == CW) {
@@ -1228,9 +1279,12 @@ __global__ void __launch_bounds__((CW + 1) * 32, RT == 32 ? 1 : 2)
         const uint64_t pol = l2_evict_first_policy();
         uint32_t it = 0;  // stages issued so far
         bool ok = true;
-        for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-            const int u = tile / rbs;
-            const int n0 = (tile - u * rbs) * RT;
+        for (int rr = 0; ok; ++rr) {
+            const int tile = ordered ? snake_tile(rr) : rr * (int)gridDim.x + (int)blockIdx.x;
+            if (tile >= tiles) break;
+            const int q = tile / rbs;
+            const int u = ordered ? sh->perm[q] : q;
+            const int n0 = (tile - q * rbs) * RT;
             const int e = m.uexp[u];
             const int shx = e >= s.E ? 1 : 0;
             const int row0 = (shx ? 0 : e) * s.I + n0;
@@ -1277,9 +1331,12 @@ __global__ void __launch_bounds__((CW + 1) * 32, RT == 32 ? 1 : 2)
         // ---------------- consumers ----------------
         RingPos rp{0, 0u};
         int grp = 0;
-        for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-            const int u = tile / rbs;
-            const int n0 = (tile - u * rbs) * RT;
+        for (int rr = 0;; ++rr) {
+            const int tile = ordered ? snake_tile(rr) : rr * (int)gridDim.x + (int)blockIdx.x;
+            if (tile >= tiles) break;
+            const int q = tile / rbs;
+            const int u = ordered ? sh->perm[q] : q;
+            const int n0 = (tile - q * rbs) * RT;
             const int s0 = m.uoff[u], s1 = m.uoff[u + 1];
             for (int t0 = s0; t0 < s1; t0 += TC, ++grp) {
                 const int nt = min(TC, s1 - t0);

@@ -60,6 +60,23 @@ def test_qwen_locality_routings(cuda_device, qwen, routing):
     compare_tokens(cuda_device, W, Wd, x, ids, w, toks, f"qwen {routing}")
 
 
+@pytest.mark.parametrize("B,routing", [(32, None), (32, "zipf"), (64, None)])
+def test_qwen_gate_up_every_tile(cuda_device, qwen, B, routing):
+    """h of every token and slot: with experts that need more than one pass
+    the gate/up tiles are dealt heaviest expert first, and each (expert, row
+    block) must still be computed exactly once."""
+    W, Wd = qwen
+    kw = {} if routing is None else {"routing": routing}
+    x, ids, w = inputs.layer_batch(inputs.QWEN3, B, **kw)
+    counts = torch.bincount(ids.reshape(-1).long(), minlength=inputs.QWEN3.E)
+    assert int(counts.max()) > 4, "the batch must hold an expert with more than one pass"
+    h = run_gate_up(cuda_device, Wd, x, ids)
+    torch.cuda.synchronize()
+    ref = oracle_tokens(W, x, ids, w, range(B))
+    check_close(h, ref["h64"], f"qwen B={B} {routing} h")
+    assert moe.device_error(cuda_device) == 0
+
+
 def test_deepseek_sampled_tokens(cuda_device):
     cfg = inputs.DEEPSEEK_V3
     W = inputs.layer_weights(cfg, cuda_device)
