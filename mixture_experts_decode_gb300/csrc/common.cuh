@@ -73,7 +73,8 @@ __device__ __forceinline__ void e4m3x4_to_float(uint32_t w, float2& lo, float2& 
 // E8M0 scale byte -> 2^(s-127) as float (s = 0 gives the subnormal 2^-127;
 // s = 255, NaN in the format, is a precondition violation and yields inf).
 __device__ __forceinline__ float e8m0_to_float(uint32_t s) {
-    return __uint_as_float(s ? (s << 23) : 0x00400000u);
+    // s >= 1 gives bits s << 23 >= 0x00800000, above the subnormal 2^-127 (0x00400000) of s = 0
+    return __uint_as_float(max(s << 23, 0x00400000u));
 }
 
 // Two BF16 values packed in one 32-bit word -> float2 (low half first).

@@ -1032,9 +1032,14 @@ struct __align__(1024) GU4Stage {
     uint16_t x[TC][GU4_KT];                       // BF16 activations of the slice
 };
 
+// A warp's FP32 copy of x keeps each 32-element block at a stride of 36
+// floats: the two blocks that the two halves of the warp broadcast from then
+// sit in different banks.
+constexpr int GU4_XH = 36;
+
 template <int RT, int CW>
 struct GU4Shared {
-    float xf[CW][TC][GU4_KT / CW];        // per warp: its blocks of x, FP32
+    float xf[CW][TC][(GU4_KT / CW / 32) * GU4_XH];  // per warp: its blocks of x, FP32
     float part[2][CW][2][TC][RT];         // [group parity][warp][proj][token][row] partial dots
     uint64_t full[GU4_S];
     uint64_t empty[GU4_S];
@@ -1096,6 +1101,7 @@ __device__ __forceinline__ void gu4_group(const GateUpArgs& a, GU4Stage<RT>* rin
     constexpr int LPR = 32 / RT;       // lanes per row
     constexpr int KW = GU4_KT / CW;    // K elements of a warp per stage (= 32 * LPR)
     static_assert(KW == 32 * LPR, "one scale block per lane");
+    constexpr int XS = LPR * GU4_XH;   // floats per token in the warp's x copy
     const DecodeShape& s = a.s;
     float2 acc[2][NT];
 #pragma unroll
@@ -1110,20 +1116,21 @@ __device__ __forceinline__ void gu4_group(const GateUpArgs& a, GU4Stage<RT>* rin
         const int slot = rp.slot;
         if (!mbar_wait_abort(&sh->full[slot], rp.par, &sh->abort)) continue;
         const GU4Stage<RT>& st = ring[slot];
-        {  // this warp's blocks of x -> FP32: lane = (token, 4 * LPR K elements)
-            constexpr int KL = 4 * LPR;
-            const int t = lane >> 3, k = (lane & 7) * KL;
+        {  // this warp's blocks of x -> FP32: lane = (token, four K elements of each block)
+            const int t = lane >> 3, k = (lane & 7) * 4;
             if (t < NT) {
+                const uint16_t* xs = &st.x[t][warp * KW + k];
+                float* xd = xf + t * XS + k;
 #pragma unroll
                 for (int q = 0; q < LPR; ++q) {
-                    const uint2 xv = *reinterpret_cast<const uint2*>(&st.x[t][warp * KW + k + 4 * q]);
+                    const uint2 xv = *reinterpret_cast<const uint2*>(xs + q * 32);
                     const float2 lo = bf16x2_to_float2(xv.x), hi = bf16x2_to_float2(xv.y);
-                    *reinterpret_cast<float4*>(xf + t * KW + k + 4 * q) = make_float4(lo.x, lo.y, hi.x, hi.y);
+                    *reinterpret_cast<float4*>(xd + q * GU4_XH) = make_float4(lo.x, lo.y, hi.x, hi.y);
                 }
             }
         }
         __syncwarp();
-        const float* xl = xf + hb * 32;
+        const float* xl = xf + hb * GU4_XH;
         float2 part[2][NT];
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {  // two 16-byte chunks = this lane's 32 K elements
@@ -1138,7 +1145,7 @@ __device__ __forceinline__ void gu4_group(const GateUpArgs& a, GU4Stage<RT>* rin
                 for (int p = 0; p < 2; ++p) e4m3x4_to_float((&wv[p].x)[q4], wq[p][0], wq[p][1]);
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
-                    const float4 xv = *reinterpret_cast<const float4*>(xl + t * KW + c2 * 16 + q4 * 4);
+                    const float4 xv = *reinterpret_cast<const float4*>(xl + t * XS + c2 * 16 + q4 * 4);
 #pragma unroll
                     for (int p = 0; p < 2; ++p) {
                         if (c2 == 0 && q4 == 0)

@@ -101,9 +101,14 @@ def test_graph_capture(cuda_device):
     assert int(n.item()) == rn
 
 
-def test_copy_kernel(cuda_device):
-    src = torch.randint(0, 255, (1 << 22,), dtype=torch.uint8, device=cuda_device)
-    dst = torch.zeros_like(src)
-    moe.copy(dst, src)
+@pytest.mark.parametrize("nbytes", [32, 32 * 257, 1 << 22])
+def test_copy_kernel(cuda_device, nbytes):
+    """One 32-byte element, a ragged last CTA (257 elements), 4 MiB; the
+    bytes after the copied span stay untouched."""
+    gen = torch.Generator(device=cuda_device).manual_seed(nbytes)
+    src = torch.randint(0, 255, (nbytes + 4096,), dtype=torch.uint8, device=cuda_device, generator=gen)
+    dst = torch.full_like(src, 0xA5)
+    moe.copy(dst[:nbytes], src[:nbytes])
     torch.cuda.synchronize()
-    assert torch.equal(dst, src)
+    assert torch.equal(dst[:nbytes], src[:nbytes])
+    assert bool((dst[nbytes:] == 0xA5).all())
