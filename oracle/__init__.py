@@ -35,6 +35,14 @@ def _load():
         lib.oracle_moe_layer.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int,
                                          P, P, P, P, P, P, ctypes.c_int, ctypes.c_int,
                                          P, P, P, P, P, P, P, P, P, P, P, P]
+        lib.oracle_moe_layer_mx_act.restype = ctypes.c_int
+        lib.oracle_moe_layer_mx_act.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int,
+                                                P, P, P, P, P, P, ctypes.c_int, ctypes.c_int,
+                                                P, P, P, P, P, P, P, P, P, P, P]
+        lib.oracle_mx_requant.restype = ctypes.c_int
+        lib.oracle_mx_requant.argtypes = [P, ctypes.c_int64, ctypes.c_int64, P]
+        lib.oracle_e4m3_round.restype = ctypes.c_double
+        lib.oracle_e4m3_round.argtypes = [ctypes.c_double]
         lib.oracle_align_sizes.restype = ctypes.c_int
         lib.oracle_align_sizes.argtypes = [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_int64)] * 2
         lib.oracle_router_topk.restype = ctypes.c_int
@@ -114,6 +122,58 @@ def moe_layer(x_bf16, topk_ids, topk_w, w_gate, s_gate, w_up, s_up, w_down, s_do
     out = {"h": h, "h64": h64, "g64": g64, "u64": u64, "y64": y}
     if want_truth:
         out["truth64"] = t
+    return out
+
+
+def moe_layer_mx_act(x_bf16, topk_ids, topk_w, w_gate, s_gate, w_up, s_up, w_down, s_down,
+                     shared=None):
+    """The conventional path's numerics: moe_layer with x and h converted to
+    MXFP8 and back before their GEMMs (see mx_requant).  Same arguments as
+    moe_layer; returns dict(h, h64, g64, u64, y64) of the converted-x pass."""
+    lib = _load()
+    x = _c(x_bf16, np.uint16)
+    ids = _c(topk_ids, np.int32)
+    w = _c(topk_w, np.float32)
+    B, d = x.shape
+    k = ids.shape[1] if ids.ndim == 2 else 0
+    wg, sg, wu, su = (_c(a, np.uint8) for a in (w_gate, s_gate, w_up, s_up))
+    wd, sd = _c(w_down, np.uint8), _c(s_down, np.uint8)
+    E, I = wg.shape[0], wg.shape[1]
+    assert wg.shape == (E, I, d) and wu.shape == (E, I, d) and wd.shape == (E, d, I)
+    sh = [None] * 6
+    S = 0
+    if shared is not None:
+        sh = [_c(a, np.uint8) for a in shared]
+        S = 1
+    h = np.zeros((B, k + S, I), dtype=np.uint16)
+    h64 = np.zeros((B, k + S, I), dtype=np.float64)
+    g64 = np.zeros((B, k + S, I), dtype=np.float64)
+    u64 = np.zeros((B, k + S, I), dtype=np.float64)
+    y = np.zeros((B, d), dtype=np.float64)
+    rc = lib.oracle_moe_layer_mx_act(_ptr(x), B, d, _ptr(ids), _ptr(w), k, _ptr(wg), _ptr(sg), _ptr(wu),
+                                     _ptr(su), _ptr(wd), _ptr(sd), E, I, *(_ptr(a) for a in sh),
+                                     _ptr(h), _ptr(h64), _ptr(g64), _ptr(u64), _ptr(y))
+    if rc != 0:
+        raise ValueError(f"oracle_moe_layer_mx_act rejected its arguments (rc={rc})")
+    return {"h": h, "h64": h64, "g64": g64, "u64": u64, "y64": y}
+
+
+def e4m3_round(q: float) -> float:
+    """The E4M3 value nearest q (ties to the even code, saturating at 448)."""
+    return float(_load().oracle_e4m3_round(float(q)))
+
+
+def mx_requant(x_bf16) -> np.ndarray:
+    """BF16 -> MXFP8 (OCP MX v1.0: shared exponent floor(log2 max|v|) - 8 per
+    32 values along the last axis, E4M3 elements nearest-even, saturating)
+    -> BF16.  x_bf16: uint16 [..., K] BF16 bit patterns, K % 32 == 0."""
+    x = _c(x_bf16, np.uint16)
+    K = x.shape[-1]
+    rows = x.size // K if K else 0
+    out = np.zeros_like(x)
+    rc = _load().oracle_mx_requant(_ptr(x), rows, K, _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_mx_requant rejected its arguments (rc={rc})")
     return out
 
 

@@ -16,7 +16,9 @@
  *         on MoE Align & Sort and "编写对AMD设备友好的CUDA实现" (the D-C-P
  *         counting / cumsum / placement algorithm).
  *   [MX]  MXFP8 as the decode page names it: E4M3 elements with one E8M0
- *         scale per 32 consecutive elements along K (OCP MX v1.0 / OFP8).
+ *         scale per 32 consecutive elements along K (OCP MX v1.0 / OFP8);
+ *         the conversion of BF16 values to it (shared-exponent rule, nearest
+ *         E4M3 with ties to even and saturation) is that standard's.
  *
  * Parity status: every function here is pinned by tests/test_oracle_pins.py
  * (exhaustive code tables, library cross-checks, a dense SwiGLU reduction,
@@ -93,6 +95,71 @@ uint16_t oracle_bf16_round(double v) {
     return sign | (uint16_t)((u >> 16) & 0x7FFF);
 }
 
+/* -------------------------------------------- MXFP8 activation round trip --- */
+
+/* The E4M3 value nearest q (finite), ties to the even code, magnitudes
+ * beyond the largest finite value 448 saturated to 448 [MX].  E4M3 has four
+ * significant bits: for |q| in [2^e, 2^(e+1)) the spacing is 2^(e-3), and
+ * below the smallest normal 2^-6 it stays 2^-9 (subnormals).  q / spacing is
+ * exact in binary64 and rint() rounds half to even, which on this grid is
+ * the code with an even last mantissa bit. */
+double oracle_e4m3_round(double q) {
+    double a = fabs(q);
+    if (a == 0.0) return q;
+    if (a >= 448.0) return copysign(448.0, q);
+    int e;
+    frexp(a, &e);           /* floor(log2 a) = e - 1 */
+    int lead = e - 1;
+    if (lead < -6) lead = -6;
+    double spacing = ldexp(1.0, lead - 3);
+    return copysign(rint(a / spacing) * spacing, q);
+}
+
+/*
+ * BF16 -> MXFP8 -> BF16, the activation round trip of the conventional
+ * expert-centric path ("Warp decode", section "準確度改進": it converts the
+ * BF16 activations to MXFP8 and back before each grouped GEMM, a rounding
+ * floor that warp decode avoids).  The conversion is the OCP MX v1.0 one,
+ * the format the page names for its weights: for each block of 32
+ * consecutive values along K, the shared exponent is
+ *     X = floor(log2(max |v|)) - 8        (8: the exponent of E4M3's largest
+ *                                          power of two, 256),
+ * clamped to the E8M0 range [-127, 127]; each element becomes the E4M3 value
+ * nearest v / 2^X (ties to even, saturating at 448), and the result is that
+ * value times 2^X, returned as BF16 (exact unless it falls below BF16's
+ * subnormal range, then rounded to nearest even).  A block of zeros stays as
+ * it is.  in and out hold rows * K BF16 bit patterns, rows major; inputs are
+ * finite.  Returns ORACLE_ERR_ARG unless K is a positive multiple of 32.
+ */
+int oracle_mx_requant(const uint16_t* in, int64_t rows, int64_t K, uint16_t* out) {
+    if (rows < 0 || K <= 0 || K % 32) return ORACLE_ERR_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b0 = 0; b0 < K; b0 += 32) {
+            const uint16_t* v = in + r * K + b0;
+            uint16_t* o = out + r * K + b0;
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i) {
+                double a = fabs(oracle_bf16_to_double(v[i]));
+                if (a > amax) amax = a;
+            }
+            if (amax == 0.0) {
+                for (int i = 0; i < 32; ++i) o[i] = v[i];
+                continue;
+            }
+            int e;
+            frexp(amax, &e);
+            int X = (e - 1) - 8;
+            if (X < -127) X = -127;
+            if (X > 127) X = 127;
+            for (int i = 0; i < 32; ++i) {
+                double q = ldexp(oracle_bf16_to_double(v[i]), -X);
+                o[i] = oracle_bf16_round(ldexp(oracle_e4m3_round(q), X));
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
 /* ---------------------------------------------------------------- [WD] --- */
 
 static double silu(double g) { return g / (1.0 + exp(-g)); }
@@ -152,26 +219,32 @@ static void down_one(const double* hv, int64_t I, const uint8_t* wd, const uint8
  * expert has the same I and d as the routed ones.
  * Returns ORACLE_ERR_ARG on a bad shape or an expert id outside [0, E).
  */
-int oracle_moe_layer(const uint16_t* x, int B, int d, const int32_t* topk_ids, const float* topk_w,
-                     int k, const uint8_t* wg, const uint8_t* sg, const uint8_t* wu,
-                     const uint8_t* su, const uint8_t* wd, const uint8_t* sd, int E, int I,
-                     const uint8_t* shg, const uint8_t* shsg, const uint8_t* shu,
-                     const uint8_t* shsu, const uint8_t* shd, const uint8_t* shsd,
-                     uint16_t* h_bf16, double* h64, double* g64, double* u64, double* y64,
-                     double* truth64) {
+static int layer_impl(const uint16_t* x, int B, int d, const int32_t* topk_ids, const float* topk_w,
+                      int k, const uint8_t* wg, const uint8_t* sg, const uint8_t* wu,
+                      const uint8_t* su, const uint8_t* wd, const uint8_t* sd, int E, int I,
+                      const uint8_t* shg, const uint8_t* shsg, const uint8_t* shu,
+                      const uint8_t* shsu, const uint8_t* shd, const uint8_t* shsd,
+                      uint16_t* h_bf16, double* h64, double* g64, double* u64, double* y64,
+                      double* truth64, int mx_act) {
     if (B < 0 || d <= 0 || I <= 0 || k < 0 || E <= 0 || d % 32 || I % 32) return ORACLE_ERR_ARG;
     int S = (shg != NULL) ? 1 : 0;
     int slots = k + S;
     uint16_t* hb = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
+    uint16_t* hq = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
+    uint16_t* xq = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)d);
     double* hf = (double*)malloc(sizeof(double) * (size_t)I);
     double* hr = (double*)malloc(sizeof(double) * (size_t)I);
-    if (!hb || !hf || !hr) {
-        free(hb); free(hf); free(hr);
+    if (!hb || !hq || !xq || !hf || !hr) {
+        free(hb); free(hq); free(xq); free(hf); free(hr);
         return ORACLE_ERR_ARG;
     }
     int rc = ORACLE_OK;
     for (int b = 0; b < B && rc == ORACLE_OK; ++b) {
         const uint16_t* xb = x + (int64_t)b * d;
+        if (mx_act) {  /* the conventional path's x before the gate/up GEMM */
+            oracle_mx_requant(xb, 1, d, xq);
+            xb = xq;
+        }
         double* yb = y64 + (int64_t)b * d;
         double* tb = truth64 ? truth64 + (int64_t)b * d : NULL;
         for (int o = 0; o < d; ++o) {
@@ -187,15 +260,52 @@ int oracle_moe_layer(const uint16_t* x, int B, int d, const int32_t* topk_ids, c
             gate_up_one(xb, d, shared ? shg : wg, shared ? shsg : sg, shared ? shu : wu,
                         shared ? shsu : su, I, e, hb, hf, g64 ? g64 + row0 : NULL,
                         u64 ? u64 + row0 : NULL);
-            for (int i = 0; i < I; ++i) hr[i] = oracle_bf16_to_double(hb[i]);
+            if (mx_act) {  /* ... and its h before the down GEMM */
+                oracle_mx_requant(hb, 1, I, hq);
+                for (int i = 0; i < I; ++i) hr[i] = oracle_bf16_to_double(hq[i]);
+            } else {
+                for (int i = 0; i < I; ++i) hr[i] = oracle_bf16_to_double(hb[i]);
+            }
             if (h_bf16) memcpy(h_bf16 + ((int64_t)b * slots + j) * I, hb, sizeof(uint16_t) * (size_t)I);
             if (h64) memcpy(h64 + ((int64_t)b * slots + j) * I, hf, sizeof(double) * (size_t)I);
             down_one(hr, I, shared ? shd : wd, shared ? shsd : sd, d, e, wt, yb);
             if (tb) down_one(hf, I, shared ? shd : wd, shared ? shsd : sd, d, e, wt, tb);
         }
     }
-    free(hb); free(hf); free(hr);
+    free(hb); free(hq); free(xq); free(hf); free(hr);
     return rc;
+}
+
+int oracle_moe_layer(const uint16_t* x, int B, int d, const int32_t* topk_ids, const float* topk_w,
+                     int k, const uint8_t* wg, const uint8_t* sg, const uint8_t* wu,
+                     const uint8_t* su, const uint8_t* wd, const uint8_t* sd, int E, int I,
+                     const uint8_t* shg, const uint8_t* shsg, const uint8_t* shu,
+                     const uint8_t* shsu, const uint8_t* shd, const uint8_t* shsd,
+                     uint16_t* h_bf16, double* h64, double* g64, double* u64, double* y64,
+                     double* truth64) {
+    return layer_impl(x, B, d, topk_ids, topk_w, k, wg, sg, wu, su, wd, sd, E, I, shg, shsg, shu, shsu,
+                      shd, shsd, h_bf16, h64, g64, u64, y64, truth64, 0);
+}
+
+/*
+ * The conventional expert-centric path's numerics ("Warp decode", section
+ * "準確度改進"): the same layer with x converted to MXFP8 and back before
+ * the gate/up GEMM and h (already BF16) converted the same way before the
+ * down GEMM (oracle_mx_requant, blocks of 32 along d and along I).  h_bf16,
+ * h64, g64 and u64 are those of the gate/up pass on the converted x (h_bf16
+ * before its own conversion); y64 is unrounded.  The full-precision truth
+ * to compare both paths with is oracle_moe_layer's truth64 on the original
+ * x (h kept in FP64, nothing converted).
+ */
+int oracle_moe_layer_mx_act(const uint16_t* x, int B, int d, const int32_t* topk_ids,
+                            const float* topk_w, int k, const uint8_t* wg, const uint8_t* sg,
+                            const uint8_t* wu, const uint8_t* su, const uint8_t* wd,
+                            const uint8_t* sd, int E, int I, const uint8_t* shg,
+                            const uint8_t* shsg, const uint8_t* shu, const uint8_t* shsu,
+                            const uint8_t* shd, const uint8_t* shsd, uint16_t* h_bf16, double* h64,
+                            double* g64, double* u64, double* y64) {
+    return layer_impl(x, B, d, topk_ids, topk_w, k, wg, sg, wu, su, wd, sd, E, I, shg, shsg, shu, shsu,
+                      shd, shsd, h_bf16, h64, g64, u64, y64, NULL, 1);
 }
 
 /* ---------------------------------------------------------------- [AS] --- */
