@@ -421,6 +421,21 @@ def run_router(dev, stream, ranks, cfg, B, K=200):
             "us": secs / K * 1e6}
 
 
+def run_requant(dev, stream, ranks, copy_gbs, rows=16384, K=4096, reps=50):
+    """The MXFP8 activation round trip (moe_mx_requant) on a BF16 [rows, K]
+    tensor larger than L2: read 2 B + write 2 B per value."""
+    import torch
+    import mixture_experts_decode_gb300 as moe
+    from mixture_experts_decode_gb300 import inputs
+    x = inputs.randn((rows, K), dev, "bench-requant").to(torch.bfloat16)
+    out = torch.empty_like(x)
+    secs, _ = time_steps(lambda i: moe.mx_requant(x, out), reps, 5, stream, ranks, chunk=25)
+    nbytes = 4 * rows * K
+    gbs = nbytes / (secs / reps) / 1e9
+    return {"workload": f"BF16 [{rows}, {K}] -> MXFP8 -> BF16", "us": secs / reps * 1e6, "gbs": gbs,
+            "algorithmic_bytes": nbytes, "frac_of_copy_peak": gbs / copy_gbs}
+
+
 # -------------------------------------------------------------------- arms ---
 
 def run_ours(args):
@@ -502,6 +517,7 @@ def run_ours(args):
 
     align = run_align(dev, stream, ranks)
     router = run_router(dev, stream, ranks, cfg, B)
+    requant = run_requant(dev, stream, ranks, copy_gbs)
 
     cpu = None
     if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
@@ -524,7 +540,7 @@ def run_ours(args):
         "pct_of_measured_peak": 100 * value * 1e3 / hbm_peak, "pct_of_8tbs_nominal": 100 * value / 8.0,
         "kernels": {"gate_up_us": gu_us, "gate_up_gbs": gu_gbs, "down_us": dn_us, "down_gbs": dn_gbs},
         "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clocks, "align": align,
-        "router": router, "cpu_baseline": cpu,
+        "router": router, "mx_requant": requant, "cpu_baseline": cpu,
     }
     if extra is not None:
         line["sweep"] = extra

@@ -256,6 +256,27 @@ int moe_router_topk(const float* logits, int B, int E, int k, int score, float s
                     float* topk_w, moe_stream_t stream);
 
 /*
+ * moe_mx_requant -- BF16 -> MXFP8 -> BF16, the activation round trip of the
+ * conventional expert-centric path [WD, section "準確度改進": that path
+ * converts the BF16 activations to MXFP8 and back before each grouped GEMM,
+ * which warp decode avoids].  It lets a caller build that path's numerics
+ * around moe_gate_up / moe_down (x before gate/up, h before down) and
+ * measure both against a full-precision reference.  The rule is OCP MX
+ * v1.0's: for each block of 32 consecutive values of a row, the shared
+ * exponent X = floor(log2(max |v|)) - 8 (clamped to [-127, 127]); each
+ * element becomes the E4M3 value nearest v / 2^X (ties to even, magnitudes
+ * above 448 saturated to 448), times 2^X, rounded to BF16 (exact unless it
+ * falls below BF16's subnormal range).  Blocks of zeros are unchanged.
+ *   in, out  BF16 [rows][K], row-major, 16-byte aligned; out may equal in
+ *            (in place); other overlap is undefined.  Values must be finite.
+ *   rows >= 0 (0 launches nothing); K > 0 and a multiple of 32.
+ * Errors: MOE_ERR_ARG (rows < 0, NULL with rows > 0), MOE_ERR_SHAPE (K),
+ * MOE_ERR_LIMIT (rows * K overflows), MOE_ERR_ALIGN.  Bit-exact: the result
+ * is unique.
+ */
+int moe_mx_requant(const void* in, void* out, int64_t rows, int K, moe_stream_t stream);
+
+/*
  * moe_device_error -- synchronise `stream`, then read and clear the sticky
  * device error bits (MOE_DEVERR_*) of the current device into *bits.
  * Returns MOE_ERR_DEVICE when any bit was set, MOE_OK otherwise.

@@ -7,8 +7,8 @@ raises if it has not been built -- there is no CPU fallback.
 """
 from ._lib import (MX, MoEError, align_block_size, align_block_size_static, align_sizes, copy, device_error, down, gate_up,
                    layer, layer_host, layer_host_workspace_bytes, layer_workspace_bytes, load,
-                   router_topk, version)
+                   mx_requant, router_topk, version)
 
 __all__ = ["MX", "MoEError", "align_block_size", "align_block_size_static", "align_sizes", "copy", "device_error", "down",
            "gate_up", "layer", "layer_host", "layer_host_workspace_bytes", "layer_workspace_bytes",
-           "load", "router_topk", "version"]
+           "load", "mx_requant", "router_topk", "version"]

@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "MOE_OK", -1: "MOE_ERR_ARG", -2: "MOE_ERR_SHAPE", -3: "MOE_ER
 EXPORTS = ("moe_version", "moe_strerror", "moe_gate_up", "moe_down", "moe_layer_workspace_bytes",
            "moe_layer", "moe_layer_host_workspace_bytes", "moe_layer_host", "moe_align_sizes",
            "moe_align_block_size", "moe_align_block_size_static", "moe_align_static_fits",
-           "moe_copy", "moe_device_error", "moe_router_topk")
+           "moe_copy", "moe_device_error", "moe_router_topk", "moe_mx_requant")
 
 
 class MoEError(RuntimeError):
@@ -70,6 +70,7 @@ def load(path: str = LIB_PATH):
                              ctypes.POINTER(S)], I),
         "moe_align_block_size": ([P, I, I, I, I, P, P, P, P, S, P], I),
         "moe_router_topk": ([P, I, I, I, I, ctypes.c_float, P, P, P], I),
+        "moe_mx_requant": ([P, P, ctypes.c_int64, I, P], I),
         "moe_align_block_size_static": ([P, I, I, I, I, P, P, P, P], I),
         "moe_align_static_fits": ([I, I, I], I),
         "moe_copy": ([P, P, S, P], I),
@@ -350,3 +351,20 @@ def router_topk(logits, k: int, score: str = "softmax", scale: float = 1.0, topk
     _check("moe_router_topk", lib.moe_router_topk(logits.data_ptr(), B, E, k, ROUTER_SCORES[score], float(scale),
                                                   topk_ids.data_ptr(), topk_w.data_ptr(), _stream(dev)))
     return topk_ids, topk_w
+
+
+def mx_requant(x, out=None):
+    """moe_mx_requant: BF16 [..., K] (device, contiguous, K % 32 == 0) ->
+    the same values through MXFP8 (OCP MX v1.0, blocks of 32 along the last
+    axis) and back to BF16.  out may be x itself."""
+    lib = load()
+    _need(x, "x", torch.bfloat16)
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", torch.bfloat16, x.device)
+    if out.shape != x.shape:
+        raise ValueError("out must have the shape of x")
+    K = x.shape[-1] if x.dim() else 0
+    rows = x.numel() // K if K else 0
+    _check("moe_mx_requant", lib.moe_mx_requant(x.data_ptr(), out.data_ptr(), rows, K, _stream(x.device)))
+    return out

@@ -261,6 +261,16 @@ int moe_router_topk(const float* logits, int B, int E, int k, int score, float s
     return cuda_status(launch_router(logits, B, E, k, score, scale, topk_ids, topk_w, (cudaStream_t)stream));
 }
 
+int moe_mx_requant(const void* in, void* out, int64_t rows, int K, moe_stream_t stream) {
+    if (rows < 0) return MOE_ERR_ARG;
+    if (K <= 0 || K % 32) return MOE_ERR_SHAPE;
+    if (rows > INT64_MAX / K) return MOE_ERR_LIMIT;
+    if (rows == 0) return MOE_OK;
+    if (!in || !out) return MOE_ERR_ARG;
+    if (!aligned(in, 16) || !aligned(out, 16)) return MOE_ERR_ALIGN;
+    return cuda_status(launch_mx_requant(in, out, rows, K, (cudaStream_t)stream));
+}
+
 int moe_align_sizes(int T, int k, int E, int block_size, int64_t* n_sorted, int64_t* n_blocks,
                     size_t* ws_bytes) {
     if (T < 0 || k < 1 || E < 1 || block_size < 1) return MOE_ERR_ARG;

@@ -109,3 +109,15 @@ def test_router_rejects_bad_arguments_before_launch(lib):
     assert lib.moe_router_topk(None, 4, 64, 8, 0, 1.0, good[1], good[2], None) == -1       # NULL
     assert lib.moe_router_topk(P(0x10002), 4, 64, 8, 0, 1.0, good[1], good[2], None) == -5  # alignment
     assert lib.moe_router_topk(None, 0, 64, 8, 1, 2.5, None, None, None) == 0               # B = 0
+
+
+def test_mx_requant_rejects_bad_arguments_before_launch(lib):
+    P = ctypes.c_void_p
+    a, b = P(0x10000), P(0x20000)
+    assert lib.moe_mx_requant(a, b, -1, 64, None) == -1           # rows < 0
+    assert lib.moe_mx_requant(a, b, 4, 48, None) == -2            # K not a multiple of 32
+    assert lib.moe_mx_requant(a, b, 4, 0, None) == -2             # K = 0
+    assert lib.moe_mx_requant(a, b, 1 << 62, 1 << 20, None) == -3  # rows * K overflows
+    assert lib.moe_mx_requant(None, b, 4, 64, None) == -1         # NULL
+    assert lib.moe_mx_requant(a, P(0x20008), 4, 64, None) == -5   # 16-byte alignment
+    assert lib.moe_mx_requant(None, None, 0, 64, None) == 0       # rows = 0 launches nothing
