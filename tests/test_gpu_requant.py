@@ -90,6 +90,28 @@ def test_requant_leaves_neighbours_alone(cuda_device):
     np.testing.assert_array_equal(_bits(view), oracle.mx_requant(_bits(x.cpu())))
 
 
+@pytest.mark.parametrize("kind", ["normal", "ties"])
+def test_requant_16_byte_aligned_buffers(cuda_device, kind):
+    """Buffers 16- but not 32-byte aligned take the 16-byte (four threads per
+    block) path; in place there too."""
+    x = _inputs(kind, 19, 160, 7)
+    n = x.numel()
+    src = torch.zeros(n + 16, dtype=torch.bfloat16, device=cuda_device)
+    dst = torch.full((n + 4096,), 1234.0, dtype=torch.bfloat16, device=cuda_device)
+    xin = src[8:8 + n].view(19, 160)              # +16 bytes
+    xin.copy_(x.to(cuda_device))
+    out = dst[8:8 + n].view(19, 160)
+    assert xin.data_ptr() % 32 == 16 and out.data_ptr() % 32 == 16
+    moe.mx_requant(xin, out=out)
+    torch.cuda.synchronize()
+    want = oracle.mx_requant(_bits(x))
+    np.testing.assert_array_equal(_bits(out), want)
+    assert bool((dst[:8] == 1234.0).all()) and bool((dst[8 + n:] == 1234.0).all())
+    moe.mx_requant(xin, out=xin)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(_bits(xin), want)
+
+
 def test_requant_empty(cuda_device):
     x = torch.empty((0, 64), dtype=torch.bfloat16, device=cuda_device)
     assert moe.mx_requant(x).shape == (0, 64)
