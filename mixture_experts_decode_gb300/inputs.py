@@ -11,6 +11,9 @@ Recipe (every tensor is seeded from a hash of (workload, tensor, expert)):
               (8 = the largest E4M3 exponent), clamped to [-127, 127]; scale
               byte = X + 127 (E8M0); element = E4M3 round-to-nearest-even of
               v / 2^X, saturated to +-448.  An all-zero block gets scale 127.
+              (FP4 variant, `quantize_mx4`: MXFP4, X = floor(log2 amax) - 2,
+              E2M1 nearest with ties to the even code, saturated to +-6, two
+              codes per byte with the lower K index in the low nibble.)
   * routing  (B rows, top-k of E):
       softmax_uniform  logits ~ U[0, 1), softmax, top-k, renormalised
       softmax_normal   logits ~ N(0, 1), softmax, top-k, renormalised
@@ -31,6 +34,11 @@ import torch
 E4M3_MAX = 448.0
 E4M3_EMAX = 8          # floor(log2(448))
 MX_BLOCK = 32
+E2M1_MAX = 6.0
+E2M1_EMAX = 2          # floor(log2(6))
+# E2M1 magnitudes of codes 0..7 are 0, 0.5, 1, 1.5, 2, 3, 4, 6: the midpoints
+# between neighbouring codes, and whether a tie there goes up (to the even code)
+_E2M1_STEPS = ((0.25, False), (0.75, True), (1.25, False), (1.75, True), (2.5, False), (3.5, True), (5.0, False))
 
 
 def seed_for(*parts) -> int:
@@ -67,6 +75,39 @@ def quantize_mx(v: torch.Tensor):
     codes = scaled.to(torch.float8_e4m3fn).view(torch.uint8).reshape(v.shape)
     scales = (X + 127).to(torch.uint8)
     return codes.contiguous(), scales.contiguous()
+
+
+def quantize_mx4(v: torch.Tensor):
+    """float32 [..., K] -> (MXFP4 codes uint8 [..., K/2]: two E2M1 codes per
+    byte, the lower K index in the low nibble; E8M0 scales uint8 [..., K/32]).
+    X = floor(log2 amax) - 2 per block of 32 (2 = the largest E2M1 exponent),
+    clamped to [-127, 127]; element = E2M1 nearest v / 2^X, ties to the even
+    code, saturated to +-6; an all-zero block gets scale 127."""
+    K = v.shape[-1]
+    assert K % MX_BLOCK == 0, "K must be a multiple of 32"
+    blocks = v.reshape(*v.shape[:-1], K // MX_BLOCK, MX_BLOCK)
+    amax = blocks.abs().amax(dim=-1)
+    _, expo = torch.frexp(amax)
+    X = (expo.to(torch.int32) - 1 - E2M1_EMAX)
+    X = torch.where(amax > 0, X, torch.zeros_like(X)).clamp(-127, 127)
+    scaled = blocks.to(torch.float64) * torch.exp2(-X.to(torch.float64)).unsqueeze(-1)
+    a = scaled.abs().clamp(max=E2M1_MAX)
+    code = torch.zeros_like(a, dtype=torch.int32)
+    for t, up in _E2M1_STEPS:
+        code += (a >= t if up else a > t).to(torch.int32)
+    code = code | ((scaled < 0) & (code > 0)).to(torch.int32) << 3
+    code = code.reshape(v.shape).to(torch.uint8)
+    packed = code[..., 0::2] | (code[..., 1::2] << 4)
+    return packed.contiguous(), (X + 127).to(torch.uint8).contiguous()
+
+
+def mx4_weights(E: int, rows: int, K: int, device, *key, std=0.02):
+    """E experts of [rows, K] MXFP4 weights ([E, rows, K/2] code bytes)."""
+    codes = torch.empty((E, rows, K // 2), dtype=torch.uint8, device=device)
+    scales = torch.empty((E, rows, K // MX_BLOCK), dtype=torch.uint8, device=device)
+    for e in range(E):
+        codes[e], scales[e] = quantize_mx4(randn((rows, K), device, *key, e, std=std))
+    return codes, scales
 
 
 def mx_weights(E: int, rows: int, K: int, device, *key, std=0.02):
@@ -154,17 +195,19 @@ DEEPSEEK_V3 = LayerConfig("deepseekv3_e256_k8_d7168_i2048_shared1", 256, 8, 7168
 CONFIGS = {c.name: c for c in (TINY, QWEN3, DEEPSEEK_V3)}
 
 
-def layer_weights(cfg: LayerConfig, device="cpu", replica: int = 0):
-    """All expert weights of a layer (plus the shared expert when present)."""
-    key = (cfg.name, "replica", replica)
-    wg, sg = mx_weights(cfg.E, cfg.I, cfg.d, device, *key, "w_gate")
-    wu, su = mx_weights(cfg.E, cfg.I, cfg.d, device, *key, "w_up")
-    wd, sd = mx_weights(cfg.E, cfg.d, cfg.I, device, *key, "w_down")
+def layer_weights(cfg: LayerConfig, device="cpu", replica: int = 0, fp4: bool = False):
+    """All expert weights of a layer (plus the shared expert when present);
+    fp4=True draws the same way and packs MXFP4 (quantize_mx4) instead."""
+    key = (cfg.name, "replica", replica) + (("fp4",) if fp4 else ())
+    gen = mx4_weights if fp4 else mx_weights
+    wg, sg = gen(cfg.E, cfg.I, cfg.d, device, *key, "w_gate")
+    wu, su = gen(cfg.E, cfg.I, cfg.d, device, *key, "w_up")
+    wd, sd = gen(cfg.E, cfg.d, cfg.I, device, *key, "w_down")
     out = dict(w_gate=wg, s_gate=sg, w_up=wu, s_up=su, w_down=wd, s_down=sd, shared=None)
     if cfg.shared:
-        shg, shsg = mx_weights(1, cfg.I, cfg.d, device, *key, "shared_gate")
-        shu, shsu = mx_weights(1, cfg.I, cfg.d, device, *key, "shared_up")
-        shd, shsd = mx_weights(1, cfg.d, cfg.I, device, *key, "shared_down")
+        shg, shsg = gen(1, cfg.I, cfg.d, device, *key, "shared_gate")
+        shu, shsu = gen(1, cfg.I, cfg.d, device, *key, "shared_up")
+        shd, shsd = gen(1, cfg.d, cfg.I, device, *key, "shared_down")
         out["shared"] = (shg, shsg, shu, shsu, shd, shsd)
     return out
 

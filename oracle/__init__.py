@@ -35,6 +35,10 @@ def _load():
         lib.oracle_moe_layer.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int,
                                          P, P, P, P, P, P, ctypes.c_int, ctypes.c_int,
                                          P, P, P, P, P, P, P, P, P, P, P, P]
+        lib.oracle_moe_layer_mx4.restype = ctypes.c_int
+        lib.oracle_moe_layer_mx4.argtypes = lib.oracle_moe_layer.argtypes
+        lib.oracle_e2m1_decode.restype = ctypes.c_double
+        lib.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
         lib.oracle_moe_layer_mx_act.restype = ctypes.c_int
         lib.oracle_moe_layer_mx_act.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int,
                                                 P, P, P, P, P, P, ctypes.c_int, ctypes.c_int,
@@ -80,8 +84,13 @@ def bf16_to_float(b: int) -> float:
     return _load().oracle_bf16_to_double(int(b))
 
 
+def e2m1_decode(q: int) -> float:
+    """Value of one FP4 E2M1 code (low 4 bits of q)."""
+    return float(_load().oracle_e2m1_decode(q & 15))
+
+
 def moe_layer(x_bf16, topk_ids, topk_w, w_gate, s_gate, w_up, s_up, w_down, s_down,
-              shared=None, want_truth=False):
+              shared=None, want_truth=False, fp4=False):
     """Run the FP64 oracle layer.
 
     x_bf16: uint16 [B, d] (BF16 bit patterns); topk_ids int32 [B, k];
@@ -90,7 +99,8 @@ def moe_layer(x_bf16, topk_ids, topk_w, w_gate, s_gate, w_up, s_up, w_down, s_do
     (w_gate, s_gate, w_up, s_up, w_down, s_down) with a leading dim of 1.
     Returns dict(h=uint16 [B, k+S, I] (BF16 bits), h64=float64 [B, k+S, I]
     (unrounded intermediates), g64/u64 (the gate and up dots), y64=float64
-    [B, d], truth64=... ).
+    [B, d], truth64=... ).  fp4=True: MXFP4 weights, w_* uint8 [E, rows,
+    K/2] with two E2M1 codes per byte (the lower K index in the low nibble).
     """
     lib = _load()
     x = _c(x_bf16, np.uint16)
@@ -101,7 +111,8 @@ def moe_layer(x_bf16, topk_ids, topk_w, w_gate, s_gate, w_up, s_up, w_down, s_do
     wg, sg, wu, su = (_c(a, np.uint8) for a in (w_gate, s_gate, w_up, s_up))
     wd, sd = _c(w_down, np.uint8), _c(s_down, np.uint8)
     E, I = wg.shape[0], wg.shape[1]
-    assert wg.shape == (E, I, d) and wu.shape == (E, I, d) and wd.shape == (E, d, I)
+    cw = 2 if fp4 else 1
+    assert wg.shape == (E, I, d // cw) and wu.shape == (E, I, d // cw) and wd.shape == (E, d, I // cw)
     assert sg.shape == (E, I, d // 32) and su.shape == (E, I, d // 32) and sd.shape == (E, d, I // 32)
     sh = [None] * 6
     S = 0
@@ -114,9 +125,10 @@ def moe_layer(x_bf16, topk_ids, topk_w, w_gate, s_gate, w_up, s_up, w_down, s_do
     u64 = np.zeros((B, k + S, I), dtype=np.float64)
     y = np.zeros((B, d), dtype=np.float64)
     t = np.zeros((B, d), dtype=np.float64) if want_truth else None
-    rc = lib.oracle_moe_layer(_ptr(x), B, d, _ptr(ids), _ptr(w), k, _ptr(wg), _ptr(sg), _ptr(wu),
-                              _ptr(su), _ptr(wd), _ptr(sd), E, I, *(_ptr(a) for a in sh),
-                              _ptr(h), _ptr(h64), _ptr(g64), _ptr(u64), _ptr(y), _ptr(t))
+    fn = lib.oracle_moe_layer_mx4 if fp4 else lib.oracle_moe_layer
+    rc = fn(_ptr(x), B, d, _ptr(ids), _ptr(w), k, _ptr(wg), _ptr(sg), _ptr(wu),
+            _ptr(su), _ptr(wd), _ptr(sd), E, I, *(_ptr(a) for a in sh),
+            _ptr(h), _ptr(h64), _ptr(g64), _ptr(u64), _ptr(y), _ptr(t))
     if rc != 0:
         raise ValueError(f"oracle_moe_layer rejected its arguments (rc={rc})")
     out = {"h": h, "h64": h64, "g64": g64, "u64": u64, "y64": y}

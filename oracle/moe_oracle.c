@@ -18,7 +18,9 @@
  *   [MX]  MXFP8 as the decode page names it: E4M3 elements with one E8M0
  *         scale per 32 consecutive elements along K (OCP MX v1.0 / OFP8);
  *         the conversion of BF16 values to it (shared-exponent rule, nearest
- *         E4M3 with ties to even and saturation) is that standard's.
+ *         E4M3 with ties to even and saturation) is that standard's.  FP4
+ *         weights (the GC-MoE page names FP8/FP4 MoE operators) are read as
+ *         the same standard's MXFP4: E2M1 elements with an E8M0 scale per 32.
  *
  * Parity status: every function here is pinned by tests/test_oracle_pins.py
  * (exhaustive code tables, library cross-checks, a dense SwiGLU reduction,
@@ -56,10 +58,35 @@ double oracle_e8m0_decode(uint8_t s) {
     return ldexp(1.0, (int)s - 127);
 }
 
-/* dequantised weight element: e4m3(q) * 2^(scale-127) [MX] */
-static double deq(const uint8_t* w, const uint8_t* sc, int64_t K, int64_t row, int64_t col) {
-    return oracle_e4m3_decode(w[row * K + col]) * oracle_e8m0_decode(sc[row * (K / 32) + col / 32]);
+/* OCP FP4 E2M1 (MX v1.0): sign, 2 exponent bits (bias 1), 1 mantissa bit,
+ * no infinities or NaN; exponent field 0 is subnormal: (-1)^s * m/2. */
+double oracle_e2m1_decode(uint8_t q) {
+    int s = (q >> 3) & 1;
+    int e = (q >> 1) & 3;
+    int m = q & 1;
+    double v = (e == 0) ? (double)m / 2.0 : ldexp(1.0 + (double)m / 2.0, e - 1);
+    return s ? -v : v;
 }
+
+/* Weight formats: MXFP8 (one E4M3 code per byte, [rows][K]) and MXFP4 (two
+ * E2M1 codes per byte, [rows][K/2], the lower K index in the low nibble);
+ * both with one E8M0 scale per 32 consecutive elements along K [MX]. */
+enum { WFMT_MXFP8 = 0, WFMT_MXFP4 = 1 };
+
+/* dequantised weight element: code(row, col) * 2^(scale-127) [MX] */
+static double deq(int fmt, const uint8_t* w, const uint8_t* sc, int64_t K, int64_t row, int64_t col) {
+    double c;
+    if (fmt == WFMT_MXFP4) {
+        uint8_t byte = w[row * (K / 2) + col / 2];
+        c = oracle_e2m1_decode((col & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15));
+    } else {
+        c = oracle_e4m3_decode(w[row * K + col]);
+    }
+    return c * oracle_e8m0_decode(sc[row * (K / 32) + col / 32]);
+}
+
+/* bytes of one expert's [rows][K] weight codes */
+static int64_t wbytes(int fmt, int64_t rows, int64_t K) { return fmt == WFMT_MXFP4 ? rows * K / 2 : rows * K; }
 
 /* ------------------------------------------------------- BF16 helpers --- */
 
@@ -170,19 +197,19 @@ static double silu(double g) { return g / (1.0 + exp(-g)); }
  *  intermediate value per (token, expert, neuron); the intermediate is
  *  BF16 (the pages keep activations in BF16 throughout).
  *  hf_out (optional) receives the unrounded FP64 value. */
-static void gate_up_one(const uint16_t* xb, int64_t d, const uint8_t* wg, const uint8_t* sg,
+static void gate_up_one(int fmt, const uint16_t* xb, int64_t d, const uint8_t* wg, const uint8_t* sg,
                         const uint8_t* wu, const uint8_t* su, int64_t I, int64_t e,
                         uint16_t* h_out, double* hf_out, double* g_out, double* u_out) {
-    const uint8_t* wge = wg + e * I * d;
+    const uint8_t* wge = wg + e * wbytes(fmt, I, d);
     const uint8_t* sge = sg + e * I * (d / 32);
-    const uint8_t* wue = wu + e * I * d;
+    const uint8_t* wue = wu + e * wbytes(fmt, I, d);
     const uint8_t* sue = su + e * I * (d / 32);
     for (int64_t n = 0; n < I; ++n) {
         double g = 0.0, u = 0.0;
         for (int64_t c = 0; c < d; ++c) {
             double xv = oracle_bf16_to_double(xb[c]);
-            g += xv * deq(wge, sge, d, n, c);
-            u += xv * deq(wue, sue, d, n, c);
+            g += xv * deq(fmt, wge, sge, d, n, c);
+            u += xv * deq(fmt, wue, sue, d, n, c);
         }
         double hf = silu(g) * u;
         if (g_out) g_out[n] = g;
@@ -193,13 +220,13 @@ static void gate_up_one(const uint16_t* xb, int64_t d, const uint8_t* wg, const 
 }
 
 /* One expert's down projection of one intermediate vector, FP64. */
-static void down_one(const double* hv, int64_t I, const uint8_t* wd, const uint8_t* sd, int64_t d,
+static void down_one(int fmt, const double* hv, int64_t I, const uint8_t* wd, const uint8_t* sd, int64_t d,
                      int64_t e, double scale, double* y) {
-    const uint8_t* wde = wd + e * d * I;
+    const uint8_t* wde = wd + e * wbytes(fmt, d, I);
     const uint8_t* sde = sd + e * d * (I / 32);
     for (int64_t o = 0; o < d; ++o) {
         double acc = 0.0;
-        for (int64_t i = 0; i < I; ++i) acc += hv[i] * deq(wde, sde, I, o, i);
+        for (int64_t i = 0; i < I; ++i) acc += hv[i] * deq(fmt, wde, sde, I, o, i);
         y[o] += scale * acc;
     }
 }
@@ -225,7 +252,7 @@ static int layer_impl(const uint16_t* x, int B, int d, const int32_t* topk_ids, 
                       const uint8_t* shg, const uint8_t* shsg, const uint8_t* shu,
                       const uint8_t* shsu, const uint8_t* shd, const uint8_t* shsd,
                       uint16_t* h_bf16, double* h64, double* g64, double* u64, double* y64,
-                      double* truth64, int mx_act) {
+                      double* truth64, int mx_act, int fmt) {
     if (B < 0 || d <= 0 || I <= 0 || k < 0 || E <= 0 || d % 32 || I % 32) return ORACLE_ERR_ARG;
     int S = (shg != NULL) ? 1 : 0;
     int slots = k + S;
@@ -257,7 +284,7 @@ static int layer_impl(const uint16_t* x, int B, int d, const int32_t* topk_ids, 
             if (!shared && (e < 0 || e >= E)) { rc = ORACLE_ERR_ARG; break; }
             double wt = shared ? 1.0 : (double)topk_w[(int64_t)b * k + j];
             const int64_t row0 = ((int64_t)b * slots + j) * I;
-            gate_up_one(xb, d, shared ? shg : wg, shared ? shsg : sg, shared ? shu : wu,
+            gate_up_one(fmt, xb, d, shared ? shg : wg, shared ? shsg : sg, shared ? shu : wu,
                         shared ? shsu : su, I, e, hb, hf, g64 ? g64 + row0 : NULL,
                         u64 ? u64 + row0 : NULL);
             if (mx_act) {  /* ... and its h before the down GEMM */
@@ -268,8 +295,8 @@ static int layer_impl(const uint16_t* x, int B, int d, const int32_t* topk_ids, 
             }
             if (h_bf16) memcpy(h_bf16 + ((int64_t)b * slots + j) * I, hb, sizeof(uint16_t) * (size_t)I);
             if (h64) memcpy(h64 + ((int64_t)b * slots + j) * I, hf, sizeof(double) * (size_t)I);
-            down_one(hr, I, shared ? shd : wd, shared ? shsd : sd, d, e, wt, yb);
-            if (tb) down_one(hf, I, shared ? shd : wd, shared ? shsd : sd, d, e, wt, tb);
+            down_one(fmt, hr, I, shared ? shd : wd, shared ? shsd : sd, d, e, wt, yb);
+            if (tb) down_one(fmt, hf, I, shared ? shd : wd, shared ? shsd : sd, d, e, wt, tb);
         }
     }
     free(hb); free(hq); free(xq); free(hf); free(hr);
@@ -284,7 +311,24 @@ int oracle_moe_layer(const uint16_t* x, int B, int d, const int32_t* topk_ids, c
                      uint16_t* h_bf16, double* h64, double* g64, double* u64, double* y64,
                      double* truth64) {
     return layer_impl(x, B, d, topk_ids, topk_w, k, wg, sg, wu, su, wd, sd, E, I, shg, shsg, shu, shsu,
-                      shd, shsd, h_bf16, h64, g64, u64, y64, truth64, 0);
+                      shd, shsd, h_bf16, h64, g64, u64, y64, truth64, 0, WFMT_MXFP8);
+}
+
+/*
+ * The same layer with MXFP4 weights (E2M1 codes, two per byte, the lower K
+ * index in the low nibble; one E8M0 scale per 32 along K): wg, wu are
+ * [E][I][d/2] bytes, wd [E][d][I/2], the scales as for MXFP8.  Activations,
+ * accumulation and every output are as in oracle_moe_layer.
+ */
+int oracle_moe_layer_mx4(const uint16_t* x, int B, int d, const int32_t* topk_ids, const float* topk_w,
+                         int k, const uint8_t* wg, const uint8_t* sg, const uint8_t* wu,
+                         const uint8_t* su, const uint8_t* wd, const uint8_t* sd, int E, int I,
+                         const uint8_t* shg, const uint8_t* shsg, const uint8_t* shu,
+                         const uint8_t* shsu, const uint8_t* shd, const uint8_t* shsd,
+                         uint16_t* h_bf16, double* h64, double* g64, double* u64, double* y64,
+                         double* truth64) {
+    return layer_impl(x, B, d, topk_ids, topk_w, k, wg, sg, wu, su, wd, sd, E, I, shg, shsg, shu, shsu,
+                      shd, shsd, h_bf16, h64, g64, u64, y64, truth64, 0, WFMT_MXFP4);
 }
 
 /*
@@ -305,7 +349,7 @@ int oracle_moe_layer_mx_act(const uint16_t* x, int B, int d, const int32_t* topk
                             const uint8_t* shd, const uint8_t* shsd, uint16_t* h_bf16, double* h64,
                             double* g64, double* u64, double* y64) {
     return layer_impl(x, B, d, topk_ids, topk_w, k, wg, sg, wu, su, wd, sd, E, I, shg, shsg, shu, shsu,
-                      shd, shsd, h_bf16, h64, g64, u64, y64, NULL, 1);
+                      shd, shsd, h_bf16, h64, g64, u64, y64, NULL, 1, WFMT_MXFP8);
 }
 
 /* ---------------------------------------------------------------- [AS] --- */
