@@ -128,6 +128,27 @@ int moe_down(const void* h, int B, int k, const int32_t* topk_ids, const float* 
              moe_mx_t w_down, int E, int d, int I, const moe_mx_t* shared_down, void* y,
              moe_stream_t stream);
 
+/*
+ * moe_gate_up_fp4, moe_down_fp4 -- the two passes with MXFP4 weights: the
+ * formulas, arguments, limits and outputs of moe_gate_up / moe_down, except
+ * that each moe_mx_t's codes are E2M1 (OCP MX v1.0 FP4: 1 sign, 2 exponent
+ * bits with bias 1, 1 mantissa bit), two per byte with the lower K index in
+ * the low nibble: gate/up codes [E][I][d/2] bytes, down codes [E][d][I/2];
+ * the E8M0 scales stay one per 32 elements along K ([E][I][d/32],
+ * [E][d][I/32]).  The GC-MoE page names FP8/FP4 MoE operators; MXFP4 halves
+ * the weight bytes of MXFP8.  x and h 16-byte aligned, codes 32-byte aligned.
+ * One warp computes one output value ([WD, how the two kernels work]);
+ * tokens sharing an expert each stream its rows.  An expert id outside
+ * [0, E) sets MOE_DEVERR_EXPERT_ID, its h is written as zero and down skips
+ * the slot.
+ */
+int moe_gate_up_fp4(const void* x, int B, int d, const int32_t* topk_ids, int k, moe_mx_t w_gate,
+                    moe_mx_t w_up, int E, int I, const moe_mx_t* shared_gate,
+                    const moe_mx_t* shared_up, void* h, moe_stream_t stream);
+int moe_down_fp4(const void* h, int B, int k, const int32_t* topk_ids, const float* topk_w,
+                 moe_mx_t w_down, int E, int d, int I, const moe_mx_t* shared_down, void* y,
+                 moe_stream_t stream);
+
 /* Bytes of workspace moe_layer needs (the BF16 intermediate h). */
 int moe_layer_workspace_bytes(int B, int k, int I, int has_shared, size_t* bytes);
 

@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "MOE_OK", -1: "MOE_ERR_ARG", -2: "MOE_ERR_SHAPE", -3: "MOE_ER
 EXPORTS = ("moe_version", "moe_strerror", "moe_gate_up", "moe_down", "moe_layer_workspace_bytes",
            "moe_layer", "moe_layer_host_workspace_bytes", "moe_layer_host", "moe_align_sizes",
            "moe_align_block_size", "moe_align_block_size_static", "moe_align_static_fits",
-           "moe_copy", "moe_device_error", "moe_router_topk", "moe_mx_requant")
+           "moe_copy", "moe_device_error", "moe_router_topk", "moe_mx_requant", "moe_gate_up_fp4",
+           "moe_down_fp4")
 
 
 class MoEError(RuntimeError):
@@ -71,6 +72,8 @@ def load(path: str = LIB_PATH):
         "moe_align_block_size": ([P, I, I, I, I, P, P, P, P, S, P], I),
         "moe_router_topk": ([P, I, I, I, I, ctypes.c_float, P, P, P], I),
         "moe_mx_requant": ([P, P, ctypes.c_int64, I, P], I),
+        "moe_gate_up_fp4": ([P, I, I, P, I, MXView, MXView, I, I, MXP, MXP, P, P], I),
+        "moe_down_fp4": ([P, I, I, P, P, MXView, I, I, I, MXP, P, P], I),
         "moe_align_block_size_static": ([P, I, I, I, I, P, P, P, P], I),
         "moe_align_static_fits": ([I, I, I], I),
         "moe_copy": ([P, P, S, P], I),
@@ -106,14 +109,15 @@ def _need(t: torch.Tensor, name: str, dtype, device=None, ndim=None):
         raise ValueError(f"{name} must be contiguous")
 
 
-def _mx(m: Optional[MX], name: str, device, rows: int, K: int, E: Optional[int] = None):
+def _mx(m: Optional[MX], name: str, device, rows: int, K: int, E: Optional[int] = None, fp4: bool = False):
     if m is None:
         return None
     _need(m.w, name + ".w", torch.uint8, device, 3)
     _need(m.s, name + ".s", torch.uint8, device, 3)
     e = m.w.shape[0] if E is None else E
-    if tuple(m.w.shape) != (e, rows, K) or tuple(m.s.shape) != (e, rows, K // 32):
-        raise ValueError(f"{name}: expected codes [{e},{rows},{K}] and scales [{e},{rows},{K // 32}], "
+    kc = K // 2 if fp4 else K   # code bytes per row (MXFP4: two codes per byte)
+    if tuple(m.w.shape) != (e, rows, kc) or tuple(m.s.shape) != (e, rows, K // 32):
+        raise ValueError(f"{name}: expected codes [{e},{rows},{kc}] and scales [{e},{rows},{K // 32}], "
                          f"got {tuple(m.w.shape)} / {tuple(m.s.shape)}")
     return MXView(m.w.data_ptr(), m.s.data_ptr())
 
@@ -127,8 +131,10 @@ def version() -> int:
 
 
 def gate_up(x, topk_ids, w_gate: MX, w_up: MX, shared_gate: Optional[MX] = None,
-            shared_up: Optional[MX] = None, h: Optional[torch.Tensor] = None):
-    """Fused gate/up pass; returns h BF16 [B, k+S, I]."""
+            shared_up: Optional[MX] = None, h: Optional[torch.Tensor] = None, fp4: bool = False):
+    """Fused gate/up pass; returns h BF16 [B, k+S, I].  fp4=True: MXFP4
+    weights (codes [E, I, d/2], two E2M1 codes per byte) through
+    moe_gate_up_fp4."""
     lib = load()
     dev = x.device
     _need(x, "x", torch.bfloat16, None, 2)
@@ -136,22 +142,25 @@ def gate_up(x, topk_ids, w_gate: MX, w_up: MX, shared_gate: Optional[MX] = None,
     B, d = x.shape
     k = topk_ids.shape[1]
     E, I = w_gate.w.shape[0], w_gate.w.shape[1]
-    vg, vu = _mx(w_gate, "w_gate", dev, I, d), _mx(w_up, "w_up", dev, I, d, E)
-    sg, su = _mx(shared_gate, "shared_gate", dev, I, d, 1), _mx(shared_up, "shared_up", dev, I, d, 1)
+    vg, vu = _mx(w_gate, "w_gate", dev, I, d, None, fp4), _mx(w_up, "w_up", dev, I, d, E, fp4)
+    sg = _mx(shared_gate, "shared_gate", dev, I, d, 1, fp4)
+    su = _mx(shared_up, "shared_up", dev, I, d, 1, fp4)
     S = 1 if sg is not None else 0
     if h is None:
         h = torch.empty((B, k + S, I), dtype=torch.bfloat16, device=dev)
     _need(h, "h", torch.bfloat16, dev)
     if h.numel() != B * (k + S) * I:
         raise ValueError("h has the wrong size")
-    _check("moe_gate_up", lib.moe_gate_up(x.data_ptr(), B, d, topk_ids.data_ptr(), k, vg, vu, E, I,
-                                          _ref(sg), _ref(su), h.data_ptr(), _stream(dev)))
+    name = "moe_gate_up_fp4" if fp4 else "moe_gate_up"
+    _check(name, getattr(lib, name)(x.data_ptr(), B, d, topk_ids.data_ptr(), k, vg, vu, E, I,
+                                    _ref(sg), _ref(su), h.data_ptr(), _stream(dev)))
     return h
 
 
 def down(h, topk_ids, topk_w, w_down: MX, shared_down: Optional[MX] = None,
-         y: Optional[torch.Tensor] = None):
-    """Down pass with the routing-weighted combine folded in; returns y BF16 [B, d]."""
+         y: Optional[torch.Tensor] = None, fp4: bool = False):
+    """Down pass with the routing-weighted combine folded in; returns y BF16
+    [B, d].  fp4=True: MXFP4 weights (codes [E, d, I/2]) through moe_down_fp4."""
     lib = load()
     dev = h.device
     _need(h, "h", torch.bfloat16, None, 3)
@@ -160,14 +169,15 @@ def down(h, topk_ids, topk_w, w_down: MX, shared_down: Optional[MX] = None,
     B, KS, I = h.shape
     k = topk_ids.shape[1]
     E, d = w_down.w.shape[0], w_down.w.shape[1]
-    vd = _mx(w_down, "w_down", dev, d, I)
-    sd = _mx(shared_down, "shared_down", dev, d, I, 1)
+    vd = _mx(w_down, "w_down", dev, d, I, None, fp4)
+    sd = _mx(shared_down, "shared_down", dev, d, I, 1, fp4)
     if KS != k + (1 if sd is not None else 0):
         raise ValueError("h's middle dimension must be k (+1 with a shared expert)")
     if y is None:
         y = torch.empty((B, d), dtype=torch.bfloat16, device=dev)
     _need(y, "y", torch.bfloat16, dev)
-    _check("moe_down", lib.moe_down(h.data_ptr(), B, k, topk_ids.data_ptr(), topk_w.data_ptr(), vd,
+    name = "moe_down_fp4" if fp4 else "moe_down"
+    _check(name, getattr(lib, name)(h.data_ptr(), B, k, topk_ids.data_ptr(), topk_w.data_ptr(), vd,
                                     E, d, I, _ref(sd), y.data_ptr(), _stream(dev)))
     return y
 

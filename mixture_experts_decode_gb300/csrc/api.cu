@@ -166,6 +166,37 @@ int moe_down(const void* h, int B, int k, const int32_t* topk_ids, const float* 
                         (cudaStream_t)stream, false);
 }
 
+int moe_gate_up_fp4(const void* x, int B, int d, const int32_t* topk_ids, int k, moe_mx_t w_gate,
+                    moe_mx_t w_up, int E, int I, const moe_mx_t* shared_gate,
+                    const moe_mx_t* shared_up, void* h, moe_stream_t stream) {
+    int rc = check_decode_shape(B, k, E, d, I);
+    if (rc) return rc;
+    if ((shared_gate == nullptr) != (shared_up == nullptr)) return MOE_ERR_ARG;
+    if (B == 0) return MOE_OK;
+    if (!x || !topk_ids || !h) return MOE_ERR_ARG;
+    if ((rc = check_mx(w_gate)) || (rc = check_mx(w_up))) return rc;
+    if (shared_gate && ((rc = check_mx(*shared_gate)) || (rc = check_mx(*shared_up)))) return rc;
+    if (!aligned(x, 16) || !aligned(h, 16) || !aligned(topk_ids, 4)) return MOE_ERR_ALIGN;
+    const DecodeShape s{B, k, E, d, I, shared_gate ? 1 : 0};
+    return cuda_status(launch_gate_up_fp4(s, x, topk_ids, view(&w_gate), view(&w_up), view(shared_gate),
+                                          view(shared_up), h, (cudaStream_t)stream));
+}
+
+int moe_down_fp4(const void* h, int B, int k, const int32_t* topk_ids, const float* topk_w,
+                 moe_mx_t w_down, int E, int d, int I, const moe_mx_t* shared_down, void* y,
+                 moe_stream_t stream) {
+    int rc = check_decode_shape(B, k, E, d, I);
+    if (rc) return rc;
+    if (B == 0) return MOE_OK;
+    if (!h || !topk_ids || !topk_w || !y) return MOE_ERR_ARG;
+    if ((rc = check_mx(w_down))) return rc;
+    if (shared_down && (rc = check_mx(*shared_down))) return rc;
+    if (!aligned(h, 16) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(y, 2)) return MOE_ERR_ALIGN;
+    const DecodeShape s{B, k, E, d, I, shared_down ? 1 : 0};
+    return cuda_status(launch_down_fp4(s, h, topk_ids, topk_w, view(&w_down), view(shared_down), y,
+                                       (cudaStream_t)stream));
+}
+
 int moe_layer_workspace_bytes(int B, int k, int I, int has_shared, size_t* bytes) {
     if (!bytes || B < 0 || k < 0 || I < 0) return MOE_ERR_ARG;
     *bytes = round_up(h_bytes(B, k, I, has_shared ? 1 : 0), 256);

@@ -31,6 +31,10 @@ cudaError_t launch_down(const DecodeShape& s, const void* h, const int32_t* ids,
 cudaError_t launch_router(const float* logits, int B, int E, int k, int score, float scale, int32_t* ids, float* w,
                           cudaStream_t st);
 cudaError_t launch_mx_requant(const void* in, void* out, int64_t rows, int K, cudaStream_t st);
+cudaError_t launch_gate_up_fp4(const DecodeShape& s, const void* x, const int32_t* ids, MXView wg, MXView wu,
+                               MXView shg, MXView shu, void* h, cudaStream_t st);
+cudaError_t launch_down_fp4(const DecodeShape& s, const void* h, const int32_t* ids, const float* w, MXView wd,
+                            MXView shd, void* y, cudaStream_t st);
 // Shared-memory bytes the decode kernels need; 0 if the shape is beyond the
 // supported limits.
 size_t gate_up_smem_bytes(const DecodeShape& s);

@@ -121,3 +121,18 @@ def test_mx_requant_rejects_bad_arguments_before_launch(lib):
     assert lib.moe_mx_requant(None, b, 4, 64, None) == -1         # NULL
     assert lib.moe_mx_requant(a, P(0x20008), 4, 64, None) == -5   # 16-byte alignment
     assert lib.moe_mx_requant(None, None, 0, 64, None) == 0       # rows = 0 launches nothing
+
+
+def test_fp4_passes_reject_bad_arguments_before_launch(lib):
+    from mixture_experts_decode_gb300._lib import MXView
+    P = ctypes.c_void_p
+    mx = MXView(0x100000, 0x200000)
+    x, ids, h, w, y = P(0x300000), P(0x400000), P(0x500000), P(0x600000), P(0x700000)
+    assert lib.moe_gate_up_fp4(x, 4, 48, ids, 2, mx, mx, 8, 64, None, None, h, None) == -2      # d % 32
+    assert lib.moe_gate_up_fp4(x, 4, 64, ids, 9, mx, mx, 8, 64, None, None, h, None) == -2      # k > E
+    assert lib.moe_gate_up_fp4(x, 4, 64, ids, 2, mx, mx, 8, 64, ctypes.byref(mx), None, h, None) == -1
+    assert lib.moe_gate_up_fp4(P(0x300008), 4, 64, ids, 2, mx, mx, 8, 64, None, None, h, None) == -5
+    assert lib.moe_gate_up_fp4(None, 0, 64, None, 2, mx, mx, 8, 64, None, None, None, None) == 0  # B = 0
+    assert lib.moe_down_fp4(h, 4, 2, ids, w, mx, 8, 64, 48, None, y, None) == -2                 # I % 32
+    assert lib.moe_down_fp4(h, 4, 2, ids, None, mx, 8, 64, 64, None, y, None) == -1             # NULL
+    assert lib.moe_down_fp4(P(0x500008), 4, 2, ids, w, mx, 8, 64, 64, None, y, None) == -5

@@ -1,0 +1,109 @@
+"""GPU parity of the MXFP4-weight passes (moe_gate_up_fp4, moe_down_fp4)
+against the oracle's FP4 layer, through the C-ABI.  Tolerance as for the
+MXFP8 layer: |gpu - oracle| <= 4e-3 * max(1, |oracle|) per element and
+per-token cosine >= 0.99999 on y."""
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_decode_gb300 as moe
+import oracle
+from mixture_experts_decode_gb300 import inputs
+
+from _gpu_helpers import WEIGHT_NAMES, check_close, check_cosine
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().astype(np.uint16)
+
+
+def _dev_weights(W, dev):
+    mx = lambda a, b: moe.MX(W[a].to(dev), W[b].to(dev))
+    out = dict(gate=mx("w_gate", "s_gate"), up=mx("w_up", "s_up"), down=mx("w_down", "s_down"), shared=None)
+    if W.get("shared") is not None:
+        s = [t.to(dev) for t in W["shared"]]
+        out["shared"] = (moe.MX(s[0], s[1]), moe.MX(s[2], s[3]), moe.MX(s[4], s[5]))
+    return out
+
+
+def _run(dev, Wd, x, ids, w):
+    sh = Wd["shared"]
+    h = moe.gate_up(x.to(dev), ids.to(dev), Wd["gate"], Wd["up"], shared_gate=sh[0] if sh else None,
+                    shared_up=sh[1] if sh else None, fp4=True)
+    y = moe.down(h, ids.to(dev), w.to(dev), Wd["down"], shared_down=sh[2] if sh else None, fp4=True)
+    torch.cuda.synchronize()
+    return h, y
+
+
+def _oracle(W, x, ids, w, tokens):
+    """The FP4 oracle layer on `tokens`, passing only the experts they touch."""
+    tokens = list(tokens)
+    sub = ids[tokens].cpu().numpy()
+    uniq = sorted(set(sub.reshape(-1).tolist()))
+    remap = np.full(max(uniq) + 1, -1, np.int64)
+    remap[uniq] = np.arange(len(uniq))
+    idx = torch.tensor(uniq, dtype=torch.long)
+    host = [W[n].index_select(0, idx.to(W[n].device)).cpu().numpy() for n in WEIGHT_NAMES]
+    shared = None if W.get("shared") is None else tuple(t.cpu().numpy() for t in W["shared"])
+    return oracle.moe_layer(_bits(x[tokens]), remap[sub].astype(np.int32), w[tokens].cpu().numpy(), *host,
+                            shared=shared, fp4=True)
+
+
+def _compare(dev, W, Wd, x, ids, w, tokens, what):
+    h, y = _run(dev, Wd, x, ids, w)
+    ref = _oracle(W, x, ids, w, tokens)
+    t = torch.tensor(list(tokens), dtype=torch.long, device=dev)
+    check_close(h.index_select(0, t), ref["h64"], what + " h")
+    check_close(y.index_select(0, t), ref["y64"], what + " y")
+    check_cosine(y.index_select(0, t), ref["y64"], what + " y")
+    assert moe.device_error(dev) == 0
+
+
+@pytest.mark.parametrize("B", [1, 3, 16])
+def test_fp4_tiny_layer(cuda_device, B):
+    W = inputs.layer_weights(inputs.TINY, "cpu", fp4=True)
+    Wd = _dev_weights(W, cuda_device)
+    x, ids, w = inputs.layer_batch(inputs.TINY, B)
+    _compare(cuda_device, W, Wd, x, ids, w, range(B), f"fp4 tiny B={B}")
+
+
+@pytest.fixture(scope="module")
+def qwen4(cuda_device):
+    W = inputs.layer_weights(inputs.QWEN3, cuda_device, fp4=True)
+    return W, _dev_weights(W, cuda_device)
+
+
+@pytest.mark.parametrize("B,tokens", [(4, range(4)), (32, [0, 13, 31])])
+def test_fp4_qwen_layer(cuda_device, qwen4, B, tokens):
+    W, Wd = qwen4
+    x, ids, w = inputs.layer_batch(inputs.QWEN3, B)
+    _compare(cuda_device, W, Wd, x, ids, w, tokens, f"fp4 qwen B={B}")
+
+
+@pytest.mark.parametrize("E,k,d,I", [(5, 2, 96, 160), (3, 3, 1056, 64)])
+def test_fp4_shared_expert_and_ragged_lanes(cuda_device, E, k, d, I):
+    """A shared expert; rows whose chunk count is not a multiple of 32."""
+    cfg = inputs.LayerConfig(f"fp4_edge_{E}_{k}_{d}_{I}", E, k, d, I, True, "softmax_normal")
+    W = inputs.layer_weights(cfg, "cpu", fp4=True)
+    Wd = _dev_weights(W, cuda_device)
+    x, ids, w = inputs.layer_batch(cfg, 5)
+    _compare(cuda_device, W, Wd, x, ids, w, range(5), f"fp4 edge {E},{k},{d},{I}")
+
+
+def test_fp4_bad_expert_id_sets_flag_and_skips_slot(cuda_device):
+    W = inputs.layer_weights(inputs.TINY, "cpu", fp4=True)
+    Wd = _dev_weights(W, cuda_device)
+    x, ids, w = inputs.layer_batch(inputs.TINY, 4)
+    bad = ids.clone()
+    bad[2, 1] = inputs.TINY.E
+    moe.device_error(cuda_device)
+    _, y = _run(cuda_device, Wd, x, bad, w)
+    assert moe.device_error(cuda_device) & 1
+    fixed, w0 = ids.clone(), w.clone()
+    fixed[2, 1] = 0
+    w0[2, 1] = 0.0
+    ref = _oracle(W, x, fixed, w0, range(4))
+    check_close(y, ref["y64"], "fp4 bad id")
+    assert moe.device_error(cuda_device) == 0
