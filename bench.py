@@ -436,6 +436,56 @@ def run_requant(dev, stream, ranks, copy_gbs, rows=16384, K=4096, reps=50):
             "algorithmic_bytes": nbytes, "frac_of_copy_peak": gbs / copy_gbs}
 
 
+def run_fp4(dev, stream, ranks, cfg, B, routing, copy_gbs, K=100, n_batches=16):
+    """The MXFP4-weight passes (moe_gate_up_fp4 + moe_down_fp4) on this
+    workload with MXFP4 weights.  Algorithmic bytes count each distinct
+    expert's codes once (I*d/2 per matrix) plus its scales (I*d/32) and the
+    activations; this path streams a shared expert's rows once per token
+    that routes to it, so its achieved GB/s is a floor, not a traffic
+    figure.  A failure here leaves an "error" field instead of a number."""
+    try:
+        import torch
+        import mixture_experts_decode_gb300 as moe
+        from mixture_experts_decode_gb300 import inputs
+        W = inputs.layer_weights(cfg, dev, fp4=True)
+        mx = lambda a, b: moe.MX(W[a], W[b])
+        G, Uw, D = mx("w_gate", "s_gate"), mx("w_up", "s_up"), mx("w_down", "s_down")
+        sh = None
+        if W.get("shared") is not None:
+            s = W["shared"]
+            sh = (moe.MX(s[0], s[1]), moe.MX(s[2], s[3]), moe.MX(s[4], s[5]))
+        S = 1 if sh else 0
+        bt = []
+        nbytes = []
+        expert = cfg.I * cfg.d // 2 + cfg.I * cfg.d // 32
+        for i in range(n_batches):
+            x, ids, w = inputs.layer_batch(cfg, B, routing=routing, step=i)
+            U = int(torch.unique(ids).numel())
+            nbytes.append((U + S) * 3 * expert + 4 * B * cfg.d + 8 * B * cfg.k + 4 * B * (cfg.k + S) * cfg.I)
+            bt.append((x.to(dev), ids.to(dev), w.to(dev)))
+        h = torch.empty((B, cfg.k + S, cfg.I), dtype=torch.bfloat16, device=dev)
+        y = torch.empty((B, cfg.d), dtype=torch.bfloat16, device=dev)
+
+        def step(i):
+            x, ids, w = bt[i % n_batches]
+            moe.gate_up(x, ids, G, Uw, shared_gate=sh[0] if sh else None, shared_up=sh[1] if sh else None,
+                        h=h, fp4=True)
+            moe.down(h, ids, w, D, shared_down=sh[2] if sh else None, y=y, fp4=True)
+
+        secs, _ = time_steps(step, K, 5, stream, ranks, chunk=50)
+        mean_bytes = sum(nbytes[i % n_batches] for i in range(K)) / K
+        us = secs / K * 1e6
+        gbs = mean_bytes / (secs / K) / 1e9
+        del W, bt
+        torch.cuda.empty_cache()
+        return {"workload": f"{cfg.name} B={B} routing={routing}, MXFP4 weights (E2M1, E8M0 per 32)",
+                "kernels": "gate_up_fp4_kernel + down_fp4_kernel (one warp per output value)",
+                "us": us, "gbs": gbs, "algorithmic_bytes_mean": mean_bytes,
+                "frac_of_copy_peak": gbs / copy_gbs}
+    except Exception as exc:  # reported, never fatal to the bench line
+        return {"error": repr(exc)[:300]}
+
+
 # -------------------------------------------------------------------- arms ---
 
 def run_ours(args):
@@ -518,6 +568,7 @@ def run_ours(args):
     align = run_align(dev, stream, ranks)
     router = run_router(dev, stream, ranks, cfg, B)
     requant = run_requant(dev, stream, ranks, copy_gbs)
+    fp4 = run_fp4(dev, stream, ranks, cfg, B, args.routing, copy_gbs)
 
     cpu = None
     if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
@@ -540,7 +591,7 @@ def run_ours(args):
         "pct_of_measured_peak": 100 * value * 1e3 / hbm_peak, "pct_of_8tbs_nominal": 100 * value / 8.0,
         "kernels": {"gate_up_us": gu_us, "gate_up_gbs": gu_gbs, "down_us": dn_us, "down_gbs": dn_gbs},
         "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clocks, "align": align,
-        "router": router, "mx_requant": requant, "cpu_baseline": cpu,
+        "router": router, "mx_requant": requant, "fp4_layer": fp4, "cpu_baseline": cpu,
     }
     if extra is not None:
         line["sweep"] = extra
