@@ -6,10 +6,11 @@
 //
 // A first FP4 path, organised as the "Warp decode" page describes its two
 // kernels (section "兩個 kernel 的運作方式"): one warp per output value.
-//   gate/up: a warp owns one (token, slot, neuron), streams the gate and up
-//     rows of the slot's expert once and the token's x once for both; lanes
-//     take 16-byte chunks (32 codes = one scale block); a __shfl_xor_sync
-//     butterfly sums the lanes; lane 0 applies SiLU(g) * u and stores BF16.
+//   gate/up: a warp owns one (token, slot, neuron) and streams the gate and
+//     up rows of the slot's expert once; lanes take 16-byte chunks (32 codes
+//     = one scale block) and the matching 32 values of x, loaded for each
+//     projection (the second load hits L1); a __shfl_xor_sync butterfly sums
+//     the lanes; lane 0 applies SiLU(g) * u and stores BF16.
 //   down: a warp owns one (token, output), walks the token's experts and adds
 //     each chunk's partial dot, scaled by the block scale times the routing
 //     weight, into one FP32 accumulator per lane; one butterfly at the end.
