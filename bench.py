@@ -123,7 +123,7 @@ def load_peaks() -> dict:
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mixture_experts_decode_gb300", "csrc")
-    for name in ("common.cuh", "decode.cu"):
+    for name in ("common.cuh", "decode_common.cuh", "gate_up.cu", "down.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libmoedec.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["api.cu", "decode.cu", "align.cu", "router.cu", "requant.cu", "decode_fp4.cu"]
+SOURCES = ["api.cu", "gate_up.cu", "down.cu", "align.cu", "router.cu", "requant.cu", "decode_fp4.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
               "-I" + INCLUDE, "-I" + CSRC]
