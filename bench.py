@@ -49,7 +49,9 @@ def parse_args(argv=None):
     p.add_argument("--batch", type=int, default=32)
     p.add_argument("--routing", default="softmax_uniform")
     p.add_argument("--config", default="qwen3", choices=["qwen3", "deepseek", "tiny"])
-    p.add_argument("--sweep", action="store_true", help="also print a B / routing / config sweep")
+    p.add_argument("--no-sweep", action="store_true", help="skip the B / routing / config sweep")
+    p.add_argument("--min-seconds", type=float, default=0.5,
+                   help="repeat the K-step timed region until this much timed work (median reported)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--ref-seconds", type=float, default=90.0)
@@ -214,9 +216,14 @@ def graph_replayer(fn_steps, n_steps: int, stream):
     return g
 
 
-def time_steps(fn_steps, K: int, W: int, stream, ranks: Ranks, chunk: int = 250, sampler=None):
-    """W untimed warm-up steps, then exactly K timed steps (CUDA graphs of
-    `chunk` steps).  Returns seconds for the K steps (this rank)."""
+def time_steps(fn_steps, K: int, W: int, stream, ranks: Ranks, chunk: int = 250, sampler=None,
+               min_seconds: float = 0.0, min_repeats: int = 1, max_repeats: int = 1):
+    """W untimed warm-up steps, then the timed region: exactly K steps (CUDA
+    graphs of `chunk` steps) between CUDA events on `stream`, with a barrier
+    and a device synchronize on both sides.  The region is repeated at least
+    `min_repeats` times and until `min_seconds` of timed work, at most
+    `max_repeats` times; returns (median seconds of one K-step region, clock
+    record, all region times)."""
     import torch
     chunk = max(1, min(chunk, K))
     with torch.cuda.stream(stream):     # first calls outside capture (one-time setup)
@@ -234,24 +241,29 @@ def time_steps(fn_steps, K: int, W: int, stream, ranks: Ranks, chunk: int = 250,
         if g_wr:
             g_wr.replay()
     stream.synchronize()
-    ranks.barrier()
-    torch.cuda.synchronize()
     if sampler:
         sampler.start()
         time.sleep(0.15)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        t0.record(stream)
-        for _ in range(K // chunk):
-            g_main.replay()
-        if g_rem:
-            g_rem.replay()
-        t1.record(stream)
-    t1.synchronize()
-    torch.cuda.synchronize()
+    times = []
+    while True:
+        ranks.barrier()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for _ in range(K // chunk):
+                g_main.replay()
+            if g_rem:
+                g_rem.replay()
+            t1.record(stream)
+        t1.synchronize()
+        torch.cuda.synchronize()
+        ranks.barrier()
+        times.append(t0.elapsed_time(t1) / 1e3)
+        if len(times) >= max_repeats or (len(times) >= min_repeats and sum(times) >= min_seconds):
+            break
     clocks = sampler.stop() if sampler else None
-    ranks.barrier()
-    return t0.elapsed_time(t1) / 1e3, clocks
+    return statistics.median(times), clocks, times
 
 
 def measure_copy_peak(dev, nbytes=1 << 30, reps=10) -> float:
@@ -274,31 +286,44 @@ def measure_copy_peak(dev, nbytes=1 << 30, reps=10) -> float:
     return 2 * nbytes / best / 1e9
 
 
+def make_replicas(cfg, dev, R, start=0):
+    """Weight replicas start .. R-1 of a layer config on the device."""
+    import mixture_experts_decode_gb300 as moe
+    from mixture_experts_decode_gb300 import inputs
+    out = []
+    for r in range(start, R):
+        W = inputs.layer_weights(cfg, dev, replica=r)
+        mx = lambda a, b: moe.MX(W[a], W[b])
+        sh = None
+        if W["shared"] is not None:
+            s = W["shared"]
+            sh = (moe.MX(s[0], s[1]), moe.MX(s[2], s[3]), moe.MX(s[4], s[5]))
+        out.append((mx("w_gate", "s_gate"), mx("w_up", "s_up"), mx("w_down", "s_down"), sh))
+    return out
+
+
 class Workload:
     """Device-resident weights (R replicas) and NB batches of one layer config."""
 
-    def __init__(self, cfg, B, routing, dev, n_batches=64, min_bytes=None):
+    def __init__(self, cfg, B, routing, dev, n_batches=64, min_bytes=None, replicas=None):
         import torch
         import mixture_experts_decode_gb300 as moe
         from mixture_experts_decode_gb300 import inputs
-        self.cfg, self.B, self.dev = cfg, B, dev
+        self.cfg, self.B, self.dev, self.routing = cfg, B, dev, routing
         self.batches = [inputs.layer_batch(cfg, B, routing=routing, step=i) for i in range(n_batches)]
         self.bytes = [layer_bytes(cfg, ids, B) for _, ids, _ in self.batches]
         mean_layer = statistics.mean(b["layer"] for b in self.bytes)
         l2 = min_bytes or 4 * L2_BYTES
         # replicas so that consecutive steps stream more than 4x L2 of weights
-        self.R = max(1, math.ceil(l2 / mean_layer))
+        R = max(1, math.ceil(l2 / mean_layer))
         full = (cfg.E + (1 if cfg.shared else 0)) * 3 * cfg.I * cfg.d * 33 // 32
-        self.R = min(self.R, max(1, int(0.5 * torch.cuda.mem_get_info(dev)[0] // full)))
-        self.replicas = []
-        for r in range(self.R):
-            W = inputs.layer_weights(cfg, dev, replica=r)
-            mx = lambda a, b: moe.MX(W[a], W[b])
-            sh = None
-            if W["shared"] is not None:
-                s = W["shared"]
-                sh = (moe.MX(s[0], s[1]), moe.MX(s[2], s[3]), moe.MX(s[4], s[5]))
-            self.replicas.append((mx("w_gate", "s_gate"), mx("w_up", "s_up"), mx("w_down", "s_down"), sh))
+        R = min(R, max(1, int(0.5 * torch.cuda.mem_get_info(dev)[0] // full)))
+        if replicas is not None and len(replicas) >= R:
+            self.replicas = replicas[:R]
+        else:
+            have = list(replicas or [])
+            self.replicas = have + make_replicas(cfg, dev, R, start=len(have))
+        self.R = len(self.replicas)
         self.x = [x.to(dev) for x, _, _ in self.batches]
         self.ids = [i.to(dev) for _, i, _ in self.batches]
         self.w = [w.to(dev) for _, _, w in self.batches]
@@ -332,13 +357,15 @@ class Workload:
 
 
 def cpu_oracle_sample(wl: "Workload", seconds: float):
-    """Time the CPU oracle on the first tokens of batch 0 (~`seconds` of CPU)."""
+    """Time the CPU oracle on the first tokens of batch 0 (~`seconds` of CPU),
+    single-threaded and pinned to one host core."""
     import numpy as np
     import torch
     import oracle
     cfg = wl.cfg
     x, ids, w = wl.batches[0]
     g, u, d, sh = wl.replicas[0]
+    host_cores = sorted(os.sched_getaffinity(0))
 
     def run(tokens):
         sub = ids[:tokens]
@@ -355,54 +382,91 @@ def cpu_oracle_sample(wl: "Workload", seconds: float):
         oracle.moe_layer(xb, remap[sub.numpy()].astype(np.int32), w[:tokens].numpy(), *host, shared=shared)
         return time.perf_counter() - t0
 
-    t1 = run(1)
-    n = int(max(1, min(wl.B, seconds / max(t1, 1e-6))))
-    dt = run(n) if n > 1 else t1
+    try:
+        os.sched_setaffinity(0, {host_cores[-1]})
+        t1 = run(1)
+        n = int(max(1, min(wl.B, seconds / max(t1, 1e-6))))
+        dt = run(n) if n > 1 else t1
+    finally:
+        os.sched_setaffinity(0, set(host_cores))
     nbytes = layer_bytes(cfg, ids[:n], n)["layer"]
     return {"value": nbytes / dt / 1e12, "unit": "TB/s", "cores": 1, "kind": "oracle",
-            "sample": f"oracle (single-threaded C, FP64) on the first {n} of {wl.B} tokens of one "
-                      f"batch: {dt:.2f} s; value = that sub-batch's algorithmic layer bytes / time"}
+            "host_cores": len(host_cores), "host_cpu_count": os.cpu_count(),
+            "sample": f"oracle (single-threaded C, FP64, pinned to one host core) on the first {n} of {wl.B} "
+                      f"tokens of one batch: {dt:.2f} s; value = that sub-batch's algorithmic layer bytes / time"}
 
 
-def sweep(dev, args):
-    """Extra lines: B sweep, routing locality, DeepSeek-V3 sizes (stderr)."""
-    import torch
-    from mixture_experts_decode_gb300 import inputs
-    out = []
-    plan = [("qwen3", B, "softmax_uniform") for B in (1, 2, 4, 8, 16, 32)]
-    plan += [("qwen3", 32, r) for r in ("contiguous", "zipf")]
-    plan += [("deepseek", B, "sigmoid_scaled") for B in (1, 8, 32, 64)]
-    ranks = Ranks()
-    stream = torch.cuda.Stream(dev)
-    for name, B, routing in plan:
-        cfg = inputs.QWEN3 if name == "qwen3" else inputs.DEEPSEEK_V3
-        wl = Workload(cfg, B, routing, dev, n_batches=16)
-        K = 400 if name == "qwen3" else 100
-        secs, _ = time_steps(wl.step, K, 20, stream, ranks, chunk=100)
-        nb = wl.mean_bytes(K)
-        out.append({"config": cfg.name, "B": B, "routing": routing, "replicas": wl.R,
-                    "unique_experts": statistics.mean(b["U"] for b in wl.bytes),
-                    "us": secs / K * 1e6, "tbps": nb * K / secs / 1e12})
-        del wl
-        torch.cuda.empty_cache()
+def measure_layer(wl, stream, ranks, K, W, hbm_peak, copy_gbs, kernels=True):
+    """Layer, and optionally each pass alone, on one workload: µs and TB/s."""
+    secs, _, _ = time_steps(wl.step, K, W, stream, ranks, chunk=min(K, 250), min_seconds=0.1, min_repeats=3, max_repeats=10)
+    nb = wl.mean_bytes(K)
+    us = secs / K * 1e6
+    out = {"B": wl.B, "routing": wl.routing, "replicas": wl.R,
+           "unique_experts_mean": statistics.mean(b["U"] for b in wl.bytes),
+           "algorithmic_bytes_mean": nb, "us": us, "tbps": nb / (us * 1e-6) / 1e12,
+           "frac_of_measured_peak": nb / (us * 1e-6) / 1e9 / hbm_peak,
+           "frac_of_copy_peak": nb / (us * 1e-6) / 1e9 / copy_gbs}
+    if kernels:
+        wl.gate_up(0)
+        for name, fn in (("gate_up", wl.gate_up), ("down", wl.down)):
+            ks, _, _ = time_steps(fn, K, W, stream, ranks, chunk=min(K, 250), min_seconds=0.1, min_repeats=3, max_repeats=10)
+            kus = ks / K * 1e6
+            kb = wl.mean_bytes(K, name)
+            out[name] = {"us": kus, "gbs": kb / (kus * 1e-6) / 1e9,
+                         "frac_of_measured_peak": kb / (kus * 1e-6) / 1e9 / hbm_peak}
     return out
 
 
-def run_align(dev, stream, ranks, K=200):
+def sweep(dev, stream, ranks, hbm_peak, copy_gbs, qwen_replicas):
+    """Every decode config of the workload list: the Qwen3-style B sweep, the
+    routing-locality sweep at B=32 (with the contiguous - scattered gap) and
+    the DeepSeek-V3-style B sweep with its shared expert."""
+    import torch
+    from mixture_experts_decode_gb300 import inputs
+    out = {"qwen3": [], "locality_b32": {}, "deepseek_v3": []}
+    reps = list(qwen_replicas)
+    for B in (1, 2, 4, 8, 16, 32):
+        wl = Workload(inputs.QWEN3, B, "softmax_uniform", dev, n_batches=16, replicas=reps)
+        reps = wl.replicas if len(wl.replicas) > len(reps) else reps
+        out["qwen3"].append(measure_layer(wl, stream, ranks, 400, 20, hbm_peak, copy_gbs))
+        if B == 32:
+            out["locality_b32"]["softmax_uniform"] = out["qwen3"][-1]
+        del wl
+    for routing in ("contiguous", "zipf"):
+        wl = Workload(inputs.QWEN3, 32, routing, dev, n_batches=16, replicas=reps)
+        out["locality_b32"][routing] = measure_layer(wl, stream, ranks, 400, 20, hbm_peak, copy_gbs)
+        del wl
+    loc = out["locality_b32"]
+    loc["gap_tbps_contiguous_minus_uniform"] = loc["contiguous"]["tbps"] - loc["softmax_uniform"]["tbps"]
+    loc["gap_tbps_contiguous_minus_zipf"] = loc["contiguous"]["tbps"] - loc["zipf"]["tbps"]
+    del reps
+    torch.cuda.empty_cache()
+    ds = []
+    for B in (1, 8, 32, 64):
+        wl = Workload(inputs.DEEPSEEK_V3, B, "sigmoid_scaled", dev, n_batches=8, replicas=ds)
+        ds = wl.replicas if len(wl.replicas) > len(ds) else ds
+        out["deepseek_v3"].append(measure_layer(wl, stream, ranks, 40, 5, hbm_peak, copy_gbs))
+        del wl
+    del ds
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_align(dev, stream, ranks, routing="softmax_normal", K=200):
     import torch
     import mixture_experts_decode_gb300 as moe
     from mixture_experts_decode_gb300 import inputs
     T, k, E, bs = 16384, 8, 256, 64
-    ids = inputs.align_ids(T, k, E).to(dev)
+    ids = inputs.align_ids(T, k, E, routing).to(dev)
     ns, nb, wsb = moe.align_sizes(T, k, E, bs)
     s = torch.empty(ns, dtype=torch.int32, device=dev)
     e = torch.empty(nb, dtype=torch.int32, device=dev)
     n = torch.empty(1, dtype=torch.int32, device=dev)
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-    secs, _ = time_steps(lambda i: moe.align_block_size(ids, E, bs, s, e, n, ws), K, 20, stream, ranks,
-                         chunk=100)
+    secs, _, _ = time_steps(lambda i: moe.align_block_size(ids, E, bs, s, e, n, ws), K, 20, stream, ranks,
+                            chunk=100, min_seconds=0.1, min_repeats=3, max_repeats=10)
     nbytes = 4 * (T * k + ns + nb + 1)
-    return {"workload": "align T=16384 k=8 E=256 block_size=64 softmax_normal", "us": secs / K * 1e6,
+    return {"workload": f"align T=16384 k=8 E=256 block_size=64 {routing}", "us": secs / K * 1e6,
             "gbs": nbytes / (secs / K) / 1e9, "algorithmic_bytes": nbytes}
 
 
@@ -416,7 +480,8 @@ def run_router(dev, stream, ranks, cfg, B, K=200):
     lg = inputs.router_logits(kind, B, cfg.E, "bench-router", B).to(dev)
     ids = torch.empty((B, cfg.k), dtype=torch.int32, device=dev)
     w = torch.empty((B, cfg.k), dtype=torch.float32, device=dev)
-    secs, _ = time_steps(lambda i: moe.router_topk(lg, cfg.k, score, scale, ids, w), K, 20, stream, ranks, chunk=100)
+    secs, _, _ = time_steps(lambda i: moe.router_topk(lg, cfg.k, score, scale, ids, w), K, 20, stream, ranks,
+                            chunk=100)
     return {"workload": f"router {score} top-{cfg.k} of E={cfg.E}, B={B}" + (f" x{scale}" if score == "sigmoid" else ""),
             "us": secs / K * 1e6}
 
@@ -429,7 +494,7 @@ def run_requant(dev, stream, ranks, copy_gbs, rows=16384, K=4096, reps=50):
     from mixture_experts_decode_gb300 import inputs
     x = inputs.randn((rows, K), dev, "bench-requant").to(torch.bfloat16)
     out = torch.empty_like(x)
-    secs, _ = time_steps(lambda i: moe.mx_requant(x, out), reps, 5, stream, ranks, chunk=25)
+    secs, _, _ = time_steps(lambda i: moe.mx_requant(x, out), reps, 5, stream, ranks, chunk=25)
     nbytes = 4 * rows * K
     gbs = nbytes / (secs / reps) / 1e9
     return {"workload": f"BF16 [{rows}, {K}] -> MXFP8 -> BF16", "us": secs / reps * 1e6, "gbs": gbs,
@@ -472,7 +537,7 @@ def run_fp4(dev, stream, ranks, cfg, B, routing, copy_gbs, K=100, n_batches=16):
                         h=h, fp4=True)
             moe.down(h, ids, w, D, shared_down=sh[2] if sh else None, y=y, fp4=True)
 
-        secs, _ = time_steps(step, K, 5, stream, ranks, chunk=50)
+        secs, _, _ = time_steps(step, K, 5, stream, ranks, chunk=50)
         mean_bytes = sum(nbytes[i % n_batches] for i in range(K)) / K
         us = secs / K * 1e6
         gbs = mean_bytes / (secs / K) / 1e9
@@ -488,11 +553,57 @@ def run_fp4(dev, stream, ranks, cfg, B, routing, copy_gbs, K=100, n_batches=16):
 
 # -------------------------------------------------------------------- arms ---
 
+def run_e2e(wl, stream, ranks, K, W):
+    """The same layer through moe_layer_host (pinned host x / topk_ids /
+    topk_w in, y out; the copies inside the timed region, every step).  Two
+    streams with their own workspace and host y take alternate steps, so one
+    step's copies overlap the other's kernels, as a serving loop would run."""
+    import torch
+    import mixture_experts_decode_gb300 as moe
+    cfg, B, dev = wl.cfg, wl.B, wl.dev
+    S = 1 if cfg.shared else 0
+    xh = [x.pin_memory() for x, _, _ in wl.batches]
+    ih = [i.pin_memory() for _, i, _ in wl.batches]
+    wh = [w.pin_memory() for _, _, w in wl.batches]
+    streams = [stream, torch.cuda.Stream(dev)]
+    yh = [torch.empty((B, cfg.d), dtype=torch.bfloat16).pin_memory() for _ in streams]
+    nws = moe.layer_host_workspace_bytes(B, cfg.d, cfg.k, cfg.I, bool(S))
+    hws = [torch.empty(nws, dtype=torch.uint8, device=dev) for _ in streams]
+
+    def e2e_step(i):
+        g, u, d, sh = wl.replicas[i % wl.R]
+        j = i % len(wl.batches)
+        q = i % 2
+        with torch.cuda.stream(streams[q]):
+            moe.layer_host(xh[j], ih[j], wh[j], g, u, d, shared=sh, workspace=hws[q], y_host=yh[q], device=dev)
+
+    for i in range(max(3, W)):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    ranks.barrier()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    streams[1].wait_event(s0)
+    for i in range(K):
+        e2e_step(i)
+    done = torch.cuda.Event()
+    done.record(streams[1])
+    stream.wait_event(done)
+    s1.record(stream)
+    s1.synchronize()
+    torch.cuda.synchronize()
+    ranks.barrier()
+    secs = s0.elapsed_time(s1) / 1e3
+    _, slow, rate = aggregate(wl.mean_bytes(K) * K, secs, ranks)
+    return {"value": rate / 1e12, "unit": "TB/s", "us_per_step": slow / K * 1e6,
+            "h2d_bytes_per_step": B * cfg.d * 2 + B * cfg.k * 8, "d2h_bytes_per_step": B * cfg.d * 2,
+            "api": "moe_layer_host (pinned host x/topk_ids/topk_w -> y), two streams taking alternate steps"}
+
+
 def run_ours(args):
     import torch
     import __graft_entry__
     from mixture_experts_decode_gb300 import inputs
-    import mixture_experts_decode_gb300 as moe
 
     ranks = Ranks()
     torch.cuda.set_device(ranks.local)
@@ -503,69 +614,44 @@ def run_ours(args):
     cfg = {"qwen3": inputs.QWEN3, "deepseek": inputs.DEEPSEEK_V3, "tiny": inputs.TINY}[args.config]
     B, K, W = args.batch, args.steps, args.warmup
     peaks = load_peaks()
+    hbm_peak = peaks.get("hbm_gbs")
+    peak_src = "MEASURED_PEAKS.json hbm_gbs (burst copy), of measured"
+    if not hbm_peak:
+        hbm_peak, peak_src = 6800.0, "fallback 6.8 TB/s, of fallback"
     copy_gbs = measure_copy_peak(dev)
 
     wl = Workload(cfg, B, args.routing, dev)
     stream = torch.cuda.Stream(dev)
     sampler = ClockSampler(ranks.local)
-    secs, clocks = time_steps(wl.step, K, W, stream, ranks, sampler=sampler)
+    secs, clocks, region_times = time_steps(wl.step, K, W, stream, ranks, sampler=sampler,
+                                            min_seconds=args.min_seconds, min_repeats=5, max_repeats=1000)
     nbytes = wl.mean_bytes(K) * K
     total_bytes, slowest, rate = aggregate(nbytes, secs, ranks)
     value = rate / 1e12
     us_per_step = slowest / K * 1e6
 
-    # per-kernel durations (same inputs, kernels launched alone)
+    # each pass alone on the same inputs, timed on the stream it launches on
     kk = max(50, min(K, 1000))
     wl.gate_up(0)
-    gu_secs, _ = time_steps(wl.gate_up, kk, 10, stream, ranks)
-    dn_secs, _ = time_steps(wl.down, kk, 10, stream, ranks)
+    gu_secs, _, _ = time_steps(wl.gate_up, kk, 10, stream, ranks, min_seconds=0.1, min_repeats=3, max_repeats=20)
+    dn_secs, _, _ = time_steps(wl.down, kk, 10, stream, ranks, min_seconds=0.1, min_repeats=3, max_repeats=20)
     gu_us, dn_us = gu_secs / kk * 1e6, dn_secs / kk * 1e6
     gu_gbs = wl.mean_bytes(kk, "gate_up") / (gu_us * 1e-6) / 1e9
     dn_gbs = wl.mean_bytes(kk, "down") / (dn_us * 1e-6) / 1e9
-    hbm_peak = peaks.get("hbm_gbs")
-    peak_src = "MEASURED_PEAKS.json hbm_gbs (burst copy)"
-    if not hbm_peak:
-        hbm_peak, peak_src = 6800.0, "fallback 6.8 TB/s"
     workload_tag = f"{args.config}_b{B}"
-    roofline = {"bound": "hbm", "kernel": "gate_up_kernel", "achieved": gu_gbs, "peak": hbm_peak,
-                "unit": "GB/s", "frac": gu_gbs / hbm_peak,
-                "traffic": profiled_traffic("gate_up", workload_tag), "peak_source": peak_src,
-                "algorithmic_bytes_per_launch": wl.mean_bytes(kk, "gate_up")}
-
-    # end to end: host activations, copies inside the timed region
-    S = 1 if cfg.shared else 0
-    xh = [x.pin_memory() for x, _, _ in wl.batches]
-    ih = [i.pin_memory() for _, i, _ in wl.batches]
-    wh = [w.pin_memory() for _, _, w in wl.batches]
-    yh = torch.empty((B, cfg.d), dtype=torch.bfloat16).pin_memory()
-    hws = torch.empty(moe.layer_host_workspace_bytes(B, cfg.d, cfg.k, cfg.I, bool(S)), dtype=torch.uint8,
-                      device=dev)
-
-    def e2e_step(i):
-        g, u, d, sh = wl.replicas[i % wl.R]
-        j = i % len(wl.batches)
-        moe.layer_host(xh[j], ih[j], wh[j], g, u, d, shared=sh, workspace=hws, y_host=yh, device=dev)
+    dom = "gate_up" if gu_us >= dn_us else "down"
+    dom_gbs = gu_gbs if dom == "gate_up" else dn_gbs
+    layer_gbs = value * 1e3
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": dom_gbs, "peak": hbm_peak, "unit": "GB/s",
+                "frac": dom_gbs / hbm_peak, "traffic": profiled_traffic(dom, workload_tag),
+                "peak_source": peak_src, "algorithmic_bytes_per_launch": wl.mean_bytes(kk, dom),
+                "layer": {"achieved": layer_gbs, "frac": layer_gbs / hbm_peak,
+                          "note": "the whole layer (both passes) against the same peak"}}
 
     Ke = min(K, 2000)
-    with torch.cuda.stream(stream):
-        for i in range(max(3, W)):
-            e2e_step(i)
-    stream.synchronize()
-    ranks.barrier()
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        s0.record(stream)
-        for i in range(Ke):
-            e2e_step(i)
-        s1.record(stream)
-    s1.synchronize()
-    e2e_secs = s0.elapsed_time(s1) / 1e3
-    _, e2e_slow, e2e_rate = aggregate(wl.mean_bytes(Ke) * Ke, e2e_secs, ranks)
-    e2e = {"value": e2e_rate / 1e12, "unit": "TB/s", "us_per_step": e2e_slow / Ke * 1e6,
-           "h2d_bytes_per_step": B * cfg.d * 2 + B * cfg.k * 8, "d2h_bytes_per_step": B * cfg.d * 2,
-           "api": "moe_layer_host (pinned host x/topk_ids/topk_w -> y)"}
-
+    e2e = run_e2e(wl, stream, ranks, Ke, W)
     align = run_align(dev, stream, ranks)
+    align_zipf = run_align(dev, stream, ranks, routing="zipf")
     router = run_router(dev, stream, ranks, cfg, B)
     requant = run_requant(dev, stream, ranks, copy_gbs)
     fp4 = run_fp4(dev, stream, ranks, cfg, B, args.routing, copy_gbs)
@@ -573,7 +659,11 @@ def run_ours(args):
     cpu = None
     if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_sample(wl, args.cpu_seconds)
-    extra = sweep(dev, args) if args.sweep else None
+    qwen_reps = wl.replicas if cfg is inputs.QWEN3 else []
+    wl_bytes = wl.bytes
+    del wl
+    torch.cuda.empty_cache()
+    sw = None if args.no_sweep else sweep(dev, stream, ranks, hbm_peak, copy_gbs, qwen_reps)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": ranks.world, "steps": K, "warmup": W,
@@ -583,18 +673,19 @@ def run_ours(args):
         "config": {"workload": f"{cfg.name} B={B} routing={args.routing}", "E": cfg.E, "k": cfg.k,
                    "d": cfg.d, "I": cfg.I, "B": B, "shared_expert": cfg.shared,
                    "weights": "MXFP8 (E4M3, E8M0 per 32 along K); BF16 activations; FP32 accumulation",
-                   "l2": f"inputs larger than L2: {wl.mean_bytes(K) / 1e6:.0f} MB streamed per step, "
-                         f"{wl.R} weight replica(s) x 64 batches cycled (L2 {L2_BYTES / 2**20:.0f} MiB)",
+                   "l2": f"inputs larger than L2: {nbytes / K / 1e6:.0f} MB streamed per step, "
+                         f"weight replicas x 64 batches cycled (L2 {L2_BYTES / 2**20:.0f} MiB)",
                    "parallelism": f"replicas x{ranks.world}"},
-        "layer_us": us_per_step, "unique_experts_mean": statistics.mean(b["U"] for b in wl.bytes),
+        "timing": {"repeats": len(region_times), "statistic": "median over repeats of the K-step region",
+                   "region_ms_min": min(region_times) * 1e3, "region_ms_max": max(region_times) * 1e3},
+        "layer_us": us_per_step, "unique_experts_mean": statistics.mean(b["U"] for b in wl_bytes),
         "copy_peak_gbs": copy_gbs, "pct_of_copy_peak": 100 * value * 1e3 / copy_gbs,
         "pct_of_measured_peak": 100 * value * 1e3 / hbm_peak, "pct_of_8tbs_nominal": 100 * value / 8.0,
         "kernels": {"gate_up_us": gu_us, "gate_up_gbs": gu_gbs, "down_us": dn_us, "down_gbs": dn_gbs},
-        "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clocks, "align": align,
-        "router": router, "mx_requant": requant, "fp4_layer": fp4, "cpu_baseline": cpu,
+        "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K * len(region_times), "clocks": clocks,
+        "align": align, "align_zipf": align_zipf, "router": router, "mx_requant": requant, "fp4_layer": fp4,
+        "cpu_baseline": cpu, "sweep": sw,
     }
-    if extra is not None:
-        line["sweep"] = extra
     if ranks.rank == 0:
         print(json.dumps(line), flush=True)
     ranks.close()
@@ -630,6 +721,8 @@ def run_reference(args):
     def step(arrs):
         oracle.moe_layer(xb, one, w1, *arrs)
 
+    host_cores = sorted(os.sched_getaffinity(0))
+    os.sched_setaffinity(0, {host_cores[-1]})   # single-threaded oracle, one pinned core
     probe = sliced(32)
     t = time.perf_counter()
     step(probe)
@@ -652,7 +745,8 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": f"{cfg.name} B={B} routing={args.routing}", "E": cfg.E, "k": cfg.k,
                        "d": cfg.d, "I": cfg.I, "B": B},
-            "cpu_baseline": {"value": value, "unit": "TB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TB/s", "cores": 1, "kind": "oracle", "sample": sample,
+                             "host_cores": len(host_cores), "host_cpu_count": os.cpu_count()},
             "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

@@ -149,13 +149,20 @@ int moe_down_fp4(const void* h, int B, int k, const int32_t* topk_ids, const flo
                  moe_mx_t w_down, int E, int d, int I, const moe_mx_t* shared_down, void* y,
                  moe_stream_t stream);
 
-/* Bytes of workspace moe_layer needs (the BF16 intermediate h). */
+/* Bytes of workspace moe_layer needs: B*(k+S)*I*4, room for the
+ * intermediate h held as FP32. */
 int moe_layer_workspace_bytes(int B, int k, int I, int has_shared, size_t* bytes);
 
 /*
- * moe_layer -- the whole decode layer: moe_gate_up then moe_down on the same
- * stream, h placed at the start of `workspace` (>= moe_layer_workspace_bytes,
- * 256-byte aligned).  Shared expert: all three shared pointers or none.
+ * moe_layer -- the whole decode layer: the gate/up pass then the down pass on
+ * the same stream, with the results of moe_gate_up followed by moe_down.
+ * The intermediate h lives at the start of `workspace` (>=
+ * moe_layer_workspace_bytes, 256-byte aligned); its layout there is internal:
+ * when I % 256 == 0 (and the weight arrays are aligned for tensor copies) it
+ * is kept as FP32 (the same BF16-rounded values) in the order the down pass
+ * reads, so that pass loads it without conversion; otherwise as the BF16
+ * [B][k+S][I] of moe_gate_up.  Shared expert: all three shared pointers or
+ * none.
  */
 int moe_layer(const void* x, int B, int d, const int32_t* topk_ids, const float* topk_w, int k,
               moe_mx_t w_gate, moe_mx_t w_up, moe_mx_t w_down, int E, int I,

@@ -201,14 +201,21 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int block_size
     const AlignPlan p = align_plan(n, E);
     int* cnt = static_cast<int*>(ws);
     const size_t smem = align_smem_bytes(E);
+    // once per device: allow the placement kernel all the opt-in shared
+    // memory (entry points may be called from several host threads)
+    static std::mutex attr_mu;
     static bool attr_done[64] = {false};
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_done[dev]) {
-        err = cudaFuncSetAttribute(align_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)(di.max_smem_optin));
-        if (err != cudaSuccess) return err;
-        attr_done[dev] = true;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(attr_mu);
+        if (!attr_done[dev]) {
+            err = cudaFuncSetAttribute(align_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)(di.max_smem_optin));
+            if (err != cudaSuccess) return err;
+            attr_done[dev] = true;
+        }
     }
     if (n > 0) {
         align_count_kernel<<<p.NB, 1024, E * sizeof(int), st>>>(ids, p.N, E, p.CH, cnt, di.err_word);

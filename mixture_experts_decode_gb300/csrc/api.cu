@@ -28,6 +28,8 @@ cudaError_t device_info(DeviceInfo* out) {
         if (err != cudaSuccess) return err;
         err = cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (err != cudaSuccess) return err;
+        err = cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        if (err != cudaSuccess) return err;
         void* p = nullptr;
         err = cudaGetSymbolAddress(&p, g_err_word);
         if (err != cudaSuccess) return err;
@@ -98,12 +100,14 @@ int check_smem(size_t need) {
 
 MXView view(const moe_mx_t* m) { return m ? MXView{m->w, m->s} : MXView{nullptr, nullptr}; }
 
-size_t h_bytes(int B, int k, int I, int S) { return (size_t)B * (k + S) * I * 2; }
+// The layer keeps its intermediate in FP32 (BF16-rounded values) when the
+// row-tile down pass takes it, else in BF16: room for the larger.
+size_t h_bytes(int B, int k, int I, int S) { return (size_t)B * (k + S) * I * 4; }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 int gate_up_checked(const void* x, int B, int d, const int32_t* ids, int k, moe_mx_t wg, moe_mx_t wu,
-                    int E, int I, const moe_mx_t* sg, const moe_mx_t* su, void* h,
+                    int E, int I, const moe_mx_t* sg, const moe_mx_t* su, void* h, bool h32,
                     cudaStream_t st) {
     int rc = check_decode_shape(B, k, E, d, I);
     if (rc) return rc;
@@ -115,10 +119,10 @@ int gate_up_checked(const void* x, int B, int d, const int32_t* ids, int k, moe_
     if (!aligned(x, 32) || !aligned(h, 32) || !aligned(ids, 4)) return MOE_ERR_ALIGN;
     const DecodeShape s{B, k, E, d, I, sg ? 1 : 0};
     if ((rc = check_smem(gate_up_smem_bytes(s)))) return rc;
-    return cuda_status(launch_gate_up(s, x, ids, view(&wg), view(&wu), view(sg), view(su), h, st));
+    return cuda_status(launch_gate_up(s, x, ids, view(&wg), view(&wu), view(sg), view(su), h, h32, st));
 }
 
-int down_checked(const void* h, int B, int k, const int32_t* ids, const float* w, moe_mx_t wd, int E,
+int down_checked(const void* h, bool h32, int B, int k, const int32_t* ids, const float* w, moe_mx_t wd, int E,
                  int d, int I, const moe_mx_t* sd, void* y, cudaStream_t st, bool pdl) {
     int rc = check_decode_shape(B, k, E, d, I);
     if (rc) return rc;
@@ -129,7 +133,7 @@ int down_checked(const void* h, int B, int k, const int32_t* ids, const float* w
     if (!aligned(h, 32) || !aligned(ids, 4) || !aligned(w, 4) || !aligned(y, 2)) return MOE_ERR_ALIGN;
     const DecodeShape s{B, k, E, d, I, sd ? 1 : 0};
     if ((rc = check_smem(down_smem_bytes(s)))) return rc;
-    return cuda_status(launch_down(s, h, ids, w, view(&wd), view(sd), y, st, pdl));
+    return cuda_status(launch_down(s, h, h32, ids, w, view(&wd), view(sd), y, st, pdl));
 }
 
 }  // namespace
@@ -155,14 +159,14 @@ const char* moe_strerror(int status) {
 int moe_gate_up(const void* x, int B, int d, const int32_t* topk_ids, int k, moe_mx_t w_gate,
                 moe_mx_t w_up, int E, int I, const moe_mx_t* shared_gate,
                 const moe_mx_t* shared_up, void* h, moe_stream_t stream) {
-    return gate_up_checked(x, B, d, topk_ids, k, w_gate, w_up, E, I, shared_gate, shared_up, h,
+    return gate_up_checked(x, B, d, topk_ids, k, w_gate, w_up, E, I, shared_gate, shared_up, h, false,
                            (cudaStream_t)stream);
 }
 
 int moe_down(const void* h, int B, int k, const int32_t* topk_ids, const float* topk_w,
              moe_mx_t w_down, int E, int d, int I, const moe_mx_t* shared_down, void* y,
              moe_stream_t stream) {
-    return down_checked(h, B, k, topk_ids, topk_w, w_down, E, d, I, shared_down, y,
+    return down_checked(h, false, B, k, topk_ids, topk_w, w_down, E, d, I, shared_down, y,
                         (cudaStream_t)stream, false);
 }
 
@@ -225,10 +229,11 @@ int moe_layer(const void* x, int B, int d, const int32_t* topk_ids, const float*
     const DecodeShape s{B, k, E, d, I, ns == 3 ? 1 : 0};
     if ((rc = check_smem(down_smem_bytes(s)))) return rc;
     cudaStream_t st = (cudaStream_t)stream;
+    const bool h32 = down_reads_h32(s, view(&w_down), view(shared_down));
     rc = gate_up_checked(x, B, d, topk_ids, k, w_gate, w_up, E, I, shared_gate, shared_up,
-                         workspace, st);
+                         workspace, h32, st);
     if (rc) return rc;
-    return down_checked(workspace, B, k, topk_ids, topk_w, w_down, E, d, I, shared_down, y, st, true);
+    return down_checked(workspace, h32, B, k, topk_ids, topk_w, w_down, E, d, I, shared_down, y, st, true);
 }
 
 int moe_layer_host_workspace_bytes(int B, int d, int k, int I, int has_shared, size_t* bytes) {

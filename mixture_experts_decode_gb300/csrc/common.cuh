@@ -118,6 +118,21 @@ __device__ __forceinline__ void cp_async_4(void* smem, const void* gmem, int src
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(a), "l"(gmem), "r"(src_bytes) : "memory");
 }
 
+// 8 bytes by cp.async (the .ca form, the only one for 8-byte copies; both
+// addresses 8-byte aligned).
+__device__ __forceinline__ void cp_async_8(void* smem, const void* gmem) {
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(a), "l"(gmem) : "memory");
+}
+
+// One arrival on `bar` once every cp.async this thread issued so far has
+// landed; the barrier's expected count must include it (.noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
 template <int N>

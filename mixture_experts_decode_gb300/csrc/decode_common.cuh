@@ -27,6 +27,7 @@ struct GateUpArgs {
     MXView wg, wu, shg, shu;
     uint16_t* h;
     int* err;
+    float* h32;  // when set, h goes here instead: FP32, in the down pass's K-slab order (h32_pos)
 };
 
 struct DownArgs {
@@ -37,8 +38,30 @@ struct DownArgs {
     MXView wd, shd;
     uint16_t* y;
     int* err;
-    int es;  // expert splits per CTA (1, 2, 4 or 8)
+    int es;            // expert splits per CTA (1, 2, 4 or 8)
+    const float* h32;  // when set, the intermediate is read from here (FP32, h32_pos order)
 };
+
+// Position of intermediate neuron n inside a row of the FP32 intermediate
+// that the gate/up pass writes for the row-tile down pass (I % 256 == 0):
+// each 256-element slab is stored as [8 groups of 4][8 lanes][4], so lane
+// kr of that pass, which owns elements kr*32 .. kr*32+31 of the slab, finds
+// its group q at float4 index q*8 + kr and the eight lanes' loads of one q
+// cover 128 consecutive bytes.
+__host__ __device__ inline int h32_pos(int n) {
+    const int w = n & 255;
+    return (n & ~255) | ((((w >> 2) & 7) * 8 + (w >> 5)) << 2) | (w & 3);
+}
+
+// Store one intermediate value: BF16 round to nearest even, then either the
+// BF16 bits at [hrow][n] of h or the same value as FP32 at h32_pos(n).
+__device__ __forceinline__ void store_h(const GateUpArgs& a, int hrow, int n, float hv) {
+    const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+    if (a.h32)
+        a.h32[(size_t)hrow * a.s.I + h32_pos(n)] = __bfloat162float(hb);
+    else
+        a.h[(size_t)hrow * a.s.I + n] = __bfloat16_as_ushort(hb);
+}
 
 // ------------------------------------------------------ routing map ------
 // Per CTA, in shared memory: the distinct experts of this call in increasing

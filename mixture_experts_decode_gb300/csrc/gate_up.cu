@@ -28,8 +28,7 @@ __device__ __forceinline__ void gate_up_rows(const uint8_t* __restrict__ wg_row,
                                              const uint8_t* __restrict__ su_row,
                                              const uint16_t* __restrict__ x, int d,
                                              const int* __restrict__ hrow_s, int KS, int cpl,
-                                             int li, bool row_ok, int n, int I,
-                                             uint16_t* __restrict__ h) {
+                                             int li, bool row_ok, int n, const GateUpArgs& a) {
     const char* xr[NT];
     int hr[NT];
 #pragma unroll
@@ -74,7 +73,7 @@ __device__ __forceinline__ void gate_up_rows(const uint8_t* __restrict__ wg_row,
         const float u = group_sum<L>(au[t].x + au[t].y);
         if (row_ok && li == (t % L)) {
             const float hv = g / (1.0f + expf(-g)) * u;
-            h[(size_t)hr[t] * I + n] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+            store_h(a, hr[t], n, hv);
         }
     }
 }
@@ -116,10 +115,10 @@ __global__ void __launch_bounds__(DEC_THREADS) gate_up_kernel(GateUpArgs a) {
             const int nt = min(TC, s1 - t0);
             const int* hs = m.hrow + t0;
             switch (nt) {
-                case 1: gate_up_rows<L, 1>(wg_row, sg_row, wu_row, su_row, a.x, s.d, hs, KS, cpl, li, row_ok, n, s.I, a.h); break;
-                case 2: gate_up_rows<L, 2>(wg_row, sg_row, wu_row, su_row, a.x, s.d, hs, KS, cpl, li, row_ok, n, s.I, a.h); break;
-                case 3: gate_up_rows<L, 3>(wg_row, sg_row, wu_row, su_row, a.x, s.d, hs, KS, cpl, li, row_ok, n, s.I, a.h); break;
-                default: gate_up_rows<L, 4>(wg_row, sg_row, wu_row, su_row, a.x, s.d, hs, KS, cpl, li, row_ok, n, s.I, a.h); break;
+                case 1: gate_up_rows<L, 1>(wg_row, sg_row, wu_row, su_row, a.x, s.d, hs, KS, cpl, li, row_ok, n, a); break;
+                case 2: gate_up_rows<L, 2>(wg_row, sg_row, wu_row, su_row, a.x, s.d, hs, KS, cpl, li, row_ok, n, a); break;
+                case 3: gate_up_rows<L, 3>(wg_row, sg_row, wu_row, su_row, a.x, s.d, hs, KS, cpl, li, row_ok, n, a); break;
+                default: gate_up_rows<L, 4>(wg_row, sg_row, wu_row, su_row, a.x, s.d, hs, KS, cpl, li, row_ok, n, a); break;
             }
         }
     }
@@ -276,7 +275,7 @@ __device__ __forceinline__ void gu2_group(const GateUpArgs& a, const RouteMap& m
 #pragma unroll
         for (int tt = 1; tt < NT; ++tt)
             if (tt == t) hrow = hr[tt];
-        a.h[(size_t)hrow * s.I + n0 + rr] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+        store_h(a, hrow, n0 + rr, hv);
     }
 }
 
@@ -438,7 +437,7 @@ __device__ __forceinline__ bool gu3_group(const GateUpArgs& a, GU3Smem* sm, uint
 #pragma unroll
         for (int tt = 1; tt < NT; ++tt)
             if (tt == t) hrow = hs[tt];
-        a.h[(size_t)hrow * s.I + n0 + 2 * cw + rr] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+        store_h(a, hrow, n0 + 2 * cw + rr, hv);
     }
     return true;
 }
@@ -701,7 +700,7 @@ __device__ __forceinline__ void gu4_group(const GateUpArgs& a, GU4Stage<RT>* rin
 #pragma unroll
             for (int tt = 1; tt < NT; ++tt)
                 if (tt == t) hrow = hs[tt];
-            a.h[(size_t)hrow * s.I + n0 + rr] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+            store_h(a, hrow, n0 + rr, hv);
         }
     }
 }
@@ -999,13 +998,14 @@ static cudaError_t launch_gate_up_v4(const GateUpArgs& a, const GU4Maps& maps, s
 
 
 cudaError_t launch_gate_up(const DecodeShape& s, const void* x, const int32_t* ids, MXView wg,
-                           MXView wu, MXView shg, MXView shu, void* h, cudaStream_t st) {
+                           MXView wu, MXView shg, MXView shu, void* h, bool h32, cudaStream_t st) {
     DeviceInfo di;
     cudaError_t err = device_info(&di);
     if (err != cudaSuccess) return err;
     int dev = 0;
-    cudaGetDevice(&dev);
-    GateUpArgs a{s, (const uint16_t*)x, ids, wg, wu, shg, shu, (uint16_t*)h, di.err_word};
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    GateUpArgs a{s, (const uint16_t*)x, ids, wg, wu, shg, shu, h32 ? nullptr : (uint16_t*)h, di.err_word,
+                 h32 ? (float*)h : nullptr};
     if (s.B >= 2 && gate_up_v4_ok(a)) {
         const size_t smem = gate_up_v4_smem(s);
         GU4Maps maps;

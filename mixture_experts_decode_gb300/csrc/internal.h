@@ -20,14 +20,19 @@ struct DecodeShape {
 struct DeviceInfo {
     int sm_count;
     int max_smem_optin;
+    int smem_per_sm;
     int* err_word;  // sticky device error bits (MOE_DEVERR_*)
 };
 cudaError_t device_info(DeviceInfo* out);
 
+// h32: the intermediate is FP32 in the row-tile down pass's order (h32_pos)
+// instead of the interface's BF16 [B][k+S][I]; the layer uses it when
+// down_reads_h32() holds for its shape and weights.
 cudaError_t launch_gate_up(const DecodeShape& s, const void* x, const int32_t* ids, MXView wg,
-                           MXView wu, MXView shg, MXView shu, void* h, cudaStream_t st);
-cudaError_t launch_down(const DecodeShape& s, const void* h, const int32_t* ids, const float* w,
+                           MXView wu, MXView shg, MXView shu, void* h, bool h32, cudaStream_t st);
+cudaError_t launch_down(const DecodeShape& s, const void* h, bool h32, const int32_t* ids, const float* w,
                         MXView wd, MXView shd, void* y, cudaStream_t st, bool after_gate_up);
+bool down_reads_h32(const DecodeShape& s, MXView wd, MXView shd);
 cudaError_t launch_router(const float* logits, int B, int E, int k, int score, float scale, int32_t* ids, float* w,
                           cudaStream_t st);
 cudaError_t launch_mx_requant(const void* in, void* out, int64_t rows, int K, cudaStream_t st);

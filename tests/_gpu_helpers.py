@@ -1,6 +1,8 @@
 """Shared helpers of the GPU parity tests (not collected by pytest)."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -109,62 +111,65 @@ def h_interval(ref, abs_g, abs_u):
     return h - dh, h + dh
 
 
-def dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
-    c = torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
-    return np.ldexp(c, np.repeat(scales.astype(np.int64) - 127, 32, axis=-1))
-
-
-class ExpertCache:
-    """Dequantised (float64) expert matrices, fetched from the weight dict."""
-
-    def __init__(self, W):
-        self.W, self.c = W, {}
-
-    def get(self, which: str, e: int):
-        key = (which, e)
-        if key not in self.c:
-            if e < 0:       # the shared expert
-                i = {"gate": 0, "up": 2, "down": 4}[which]
-                codes, scales = self.W["shared"][i][0], self.W["shared"][i + 1][0]
-            else:
-                codes, scales = self.W["w_" + which][e], self.W["s_" + which][e]
-            self.c[key] = dequant(codes.cpu().numpy(), scales.cpu().numpy())
-        return self.c[key]
+def abs_matrix(W, which: str, e: int) -> torch.Tensor:
+    """|dequantised weight matrix| of expert e (e < 0: the shared expert), FP32
+    on the CPU (exact for these weights; it only feeds error bounds)."""
+    if e < 0:
+        i = {"gate": 0, "up": 2, "down": 4}[which]
+        codes, scales = W["shared"][i][0], W["shared"][i + 1][0]
+    else:
+        codes, scales = W["w_" + which][e], W["s_" + which][e]
+    rows, K = codes.shape
+    c = codes.cpu().contiguous().view(torch.float8_e4m3fn).to(torch.float32).abs()
+    sc = torch.exp2(scales.cpu().to(torch.float32) - 127.0)
+    return (c.view(rows, K // 32, 32) * sc.view(rows, K // 32, 1)).view(rows, K)
 
 
 def _slot_expert(ids_tok, b, j, k):
     return int(ids_tok[b, j]) if j < k else -1
 
 
-def abs_sums(cache, x_tok, ids_tok, KS):
-    """sum_c |x_c * Wg[n, c]| and the same for Wu, per (token, slot, neuron)."""
+def _slots_by_expert(ids_tok, KS):
+    """{expert: [(b, j), ...]} over every slot (j == k is the shared expert, -1)."""
     T, k = ids_tok.shape
-    ax = np.abs(x_tok)
-    sg, su = [], []
+    out = {}
     for b in range(T):
-        rg, ru = [], []
         for j in range(KS):
-            e = _slot_expert(ids_tok, b, j, k)
-            rg.append(np.abs(cache.get("gate", e)) @ ax[b])
-            ru.append(np.abs(cache.get("up", e)) @ ax[b])
-        sg.append(rg)
-        su.append(ru)
-    return np.array(sg), np.array(su)
+            out.setdefault(_slot_expert(ids_tok, b, j, k), []).append((b, j))
+    return out
 
 
-def y_allowance(cache, ids_tok, w_tok, gap):
+def abs_sums(W, x_tok, ids_tok, KS):
+    """sum_c |x_c * Wg[n, c]| and the same for Wu, per (token, slot, neuron);
+    one expert's matrices at a time."""
+    T = ids_tok.shape[0]
+    ax = torch.from_numpy(np.abs(x_tok)).to(torch.float32)
+    sg = su = None
+    for e, slots in _slots_by_expert(ids_tok, KS).items():
+        bs = [b for b, _ in slots]
+        g = (abs_matrix(W, "gate", e) @ ax[bs].T).T.double().numpy()
+        u = (abs_matrix(W, "up", e) @ ax[bs].T).T.double().numpy()
+        if sg is None:
+            sg = np.zeros((T, KS, g.shape[1]))
+            su = np.zeros_like(sg)
+        for i, (b, j) in enumerate(slots):
+            sg[b, j], su[b, j] = g[i], u[i]
+    return sg, su
+
+
+def y_allowance(W, ids_tok, w_tok, gap, d):
     """Per-output allowance for the h whose BF16 rounding is not unique."""
     T, KS, I = gap.shape
     k = ids_tok.shape[1]
-    d = cache.get("down", _slot_expert(ids_tok, 0, 0, k)).shape[0]
     allow = np.zeros((T, d))
-    for b in range(T):
-        for j in range(KS):
-            if not np.any(gap[b, j]):
-                continue
-            e = _slot_expert(ids_tok, b, j, k)
+    for e, slots in _slots_by_expert(ids_tok, KS).items():
+        slots = [(b, j) for b, j in slots if np.any(gap[b, j])]
+        if not slots:
+            continue
+        A = abs_matrix(W, "down", e)
+        for b, j in slots:
             wt = abs(float(w_tok[b, j])) if j < k else 1.0
-            allow[b] += wt * (np.abs(cache.get("down", e)) @ gap[b, j])
+            allow[b] += wt * (A @ torch.from_numpy(gap[b, j]).to(torch.float32)).double().numpy()
     return allow
 
 
@@ -193,26 +198,100 @@ def run_gate_up(dev, Wd, x, ids):
                        shared_gate=sh[0] if sh else None, shared_up=sh[1] if sh else None)
 
 
-def compare_tokens(dev, W, Wd, x, ids, w, tokens, what):
-    """GPU layer on the whole batch vs the oracle on `tokens`; checks h and y."""
+def check_plain(got: torch.Tensor, ref64: np.ndarray, what: str, allow=None) -> float:
+    """The plain bar |gpu - y64| <= TOL * max(1, |y64|), plus `allow` where
+    given (the effect of h values the GPU rounded the other valid way)."""
+    g = got.detach().float().cpu().double().numpy().reshape(ref64.shape)
+    err = np.abs(g - ref64)
+    scaled = err / np.maximum(1.0, np.abs(ref64))
+    worst = float(scaled.max()) if scaled.size else 0.0
+    if allow is None:
+        assert worst <= TOL, f"{what}: max plain scaled error {worst:.3e} > {TOL}"
+    else:
+        excess = (np.maximum(err - allow, 0.0) / np.maximum(1.0, np.abs(ref64))).max()
+        assert excess <= TOL, (f"{what}: max scaled error beyond the rounding differences of h "
+                               f"{excess:.3e} > {TOL} (plain {worst:.3e})")
+    return worst
+
+
+def _report(line: str):
+    path = os.environ.get("MOEDEC_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(line + "\n")
+
+
+def compare_tokens(dev, W, Wd, x, ids, w, tokens, what, chunk=8, plain=True):
+    """GPU layer on the whole batch vs the oracle on `tokens` (in chunks of
+    `chunk` tokens, so only their experts are held on the host); checks h
+    (valid BF16 rounding), y against the tolerance with the rounding
+    allowance, y against the plain tolerance, and the per-token cosine.
+
+    plain=False (layers whose y reach |y| > 1, where BF16 rounding of y alone
+    may take 3.906e-3 of the 4e-3): y must meet the plain tolerance plus the
+    exact effect of the h values where the GPU's BF16 rounding differs from
+    the oracle's (both valid: the exact h lies within FP32 error of a BF16
+    midpoint), i.e. sum_j |w_j| sum_i |Wd[e_j, o, i]| |h_gpu - h_oracle|_i;
+    with no such h it is the plain bar itself."""
     y = run_layer(dev, Wd, x, ids, w)
     h = run_gate_up(dev, Wd, x, ids)
     torch.cuda.synchronize()
-    ref = oracle_tokens(W, x, ids, w, tokens)
-    t = torch.tensor(list(tokens), dtype=torch.long, device=dev)
-    toks = list(tokens)
-    ids_tok, w_tok = ids[toks].cpu().numpy(), w[toks].cpu().numpy()
-    x_tok = x[toks].float().double().numpy()
-    cache = ExpertCache(W)
-    KS = ref["h"].shape[1]
-    ag, au = abs_sums(cache, x_tok, ids_tok, KS)
-    lo, hi = h_interval(ref, ag, au)
-    gap = check_h(h.index_select(0, t), ref, lo, hi, what + " h")
-    allow = y_allowance(cache, ids_tok, w_tok, gap) if np.any(gap) else None
-    e_y = check_close(y.index_select(0, t), ref["y64"], what + " y", allow)
-    c = check_cosine(y.index_select(0, t), ref["y64"], what + " y")
     assert moe.device_error(dev) == 0
-    return int(np.count_nonzero(gap)), e_y, c
+    tokens = list(tokens)
+    d = y.shape[1]
+    n_gap, n_diff, worst, worst_plain, cos_min = 0, 0, 0.0, 0.0, 1.0
+    for c0 in range(0, len(tokens), chunk):
+        toks = tokens[c0:c0 + chunk]
+        ref = oracle_tokens(W, x, ids, w, toks)
+        t = torch.tensor(toks, dtype=torch.long, device=dev)
+        ids_tok, w_tok = ids[toks].cpu().numpy(), w[toks].cpu().numpy()
+        x_tok = x[toks].float().double().numpy()
+        KS = ref["h"].shape[1]
+        ag, au = abs_sums(W, x_tok, ids_tok, KS)
+        lo, hi = h_interval(ref, ag, au)
+        ht = h.index_select(0, t)
+        gap = check_h(ht, ref, lo, hi, what + " h")
+        allow = y_allowance(W, ids_tok, w_tok, gap, d) if np.any(gap) else None
+        yt = y.index_select(0, t)
+        worst = max(worst, check_close(yt, ref["y64"], what + " y", allow))
+        diff = np.abs(_bf16_value(bf16_bits(ht).reshape(ref["h"].shape)) - _bf16_value(ref["h"]))
+        n_diff += int(np.count_nonzero(diff))
+        obs = None
+        if not plain and np.any(diff):
+            obs = y_allowance(W, ids_tok, w_tok, diff, d)
+        worst_plain = max(worst_plain, check_plain(yt, ref["y64"], what + " y", None if plain else obs))
+        cos_min = min(cos_min, check_cosine(yt, ref["y64"], what + " y"))
+        n_gap += int(np.count_nonzero(gap))
+    _report(f"{what}: tokens {len(tokens)}/{x.shape[0]}, max plain scaled error {worst_plain:.3e} "
+            f"({'asserted' if plain else 'asserted beyond the observed h rounding differences'}), "
+            f"with allowance {worst:.3e}, min cosine {cos_min:.8f}, h with two valid roundings {n_gap}, "
+            f"h rounded the other valid way {n_diff}")
+    return n_gap, worst_plain, cos_min
+
+
+def item_cover(ids, shared: bool, tc: int = 4):
+    """Tokens such that every work item of the decode passes, (expert, group
+    of tc of its tokens in increasing order), holds at least one of them:
+    a greedy set cover."""
+    ids = np.asarray(ids)
+    B = ids.shape[0]
+    groups = []
+    for e in sorted(set(ids.reshape(-1).tolist())):
+        toks = sorted(set(np.nonzero((ids == e).any(1))[0].tolist()))
+        groups += [set(toks[i:i + tc]) for i in range(0, len(toks), tc)]
+    if shared:
+        groups += [set(range(i, min(B, i + tc))) for i in range(0, B, tc)]
+    chosen = set()
+    left = [g for g in groups]
+    while left:
+        counts = {}
+        for g in left:
+            for b in g:
+                counts[b] = counts.get(b, 0) + 1
+        best = min(counts, key=lambda b: (-counts[b], b))
+        chosen.add(best)
+        left = [g for g in left if best not in g]
+    return sorted(chosen)
 
 
 def small_weights(E, d, I, shared, seed, dev="cpu"):

@@ -70,7 +70,7 @@ def test_down_and_layer_reject_bad_arguments(lib):
     assert lib.moe_down(0x40000, 2, 2, 0x30000, None, m, 4, 64, 64, None, 0x60000, None) == -1
     ws = ctypes.c_size_t()
     assert lib.moe_layer_workspace_bytes(4, 8, 768, 1, ctypes.byref(ws)) == 0
-    assert ws.value == 4 * 9 * 768 * 2
+    assert ws.value == 4 * 9 * 768 * 4                  # FP32 intermediate, [B][k+S][I]
     assert lib.moe_layer_workspace_bytes(4, 8, 768, 0, ctypes.byref(ws)) == 0
     small = ws.value - 1
     rc = lib.moe_layer(0x20000, 4, 2048, 0x30000, 0x50000, 8, m, m, m, 16, 768, None, None, None,

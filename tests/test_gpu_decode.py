@@ -7,8 +7,8 @@ import torch
 import mixture_experts_decode_gb300 as moe
 from mixture_experts_decode_gb300 import inputs
 
-from _gpu_helpers import (check_close, check_cosine, compare_tokens, device_mx, oracle_tokens,
-                          run_gate_up, run_layer, small_weights)
+from _gpu_helpers import (check_close, compare_tokens, device_mx, item_cover, oracle_tokens, run_gate_up,
+                          run_layer, small_weights)
 
 pytestmark = pytest.mark.gpu
 
@@ -40,24 +40,31 @@ def test_qwen_full_batch(cuda_device, qwen, B):
 
 
 @pytest.mark.parametrize("B", [8, 16, 32])
-def test_qwen_sampled_tokens(cuda_device, qwen, B):
+def test_qwen_every_token(cuda_device, qwen, B):
     W, Wd = qwen
     x, ids, w = inputs.layer_batch(inputs.QWEN3, B)
-    compare_tokens(cuda_device, W, Wd, x, ids, w, sorted({0, B // 2, B - 1}), f"qwen B={B}")
+    compare_tokens(cuda_device, W, Wd, x, ids, w, range(B), f"qwen B={B}")
 
 
 @pytest.mark.parametrize("routing", ["contiguous", "zipf", "softmax_uniform"])
 def test_qwen_locality_routings(cuda_device, qwen, routing):
+    """Every token of the B=32 batch under each routing of the locality sweep."""
     W, Wd = qwen
     B = 32
     x, ids, w = inputs.layer_batch(inputs.QWEN3, B, routing=routing)
     if routing == "contiguous":
         assert inputs.unique_experts(ids) == 128
-    # the hottest expert's tokens plus the first and last token
-    flat = ids.reshape(-1)
-    hot = int(torch.mode(flat).values)
-    toks = sorted({0, B - 1, int((ids == hot).any(1).nonzero()[0, 0])})
-    compare_tokens(cuda_device, W, Wd, x, ids, w, toks, f"qwen {routing}")
+    compare_tokens(cuda_device, W, Wd, x, ids, w, range(B), f"qwen B=32 {routing}")
+
+
+@pytest.mark.parametrize("B", [64, 256])
+def test_qwen_large_batch_item_cover(cuda_device, qwen, B):
+    """Above the decode batches: one token of every (expert, 4-token group)
+    work item, so every item of both passes meets the oracle."""
+    W, Wd = qwen
+    x, ids, w = inputs.layer_batch(inputs.QWEN3, B)
+    toks = item_cover(ids.numpy(), False)
+    compare_tokens(cuda_device, W, Wd, x, ids, w, toks, f"qwen B={B} item cover")
 
 
 @pytest.mark.parametrize("B,routing", [(32, None), (32, "zipf"), (64, None)])
@@ -77,15 +84,29 @@ def test_qwen_gate_up_every_tile(cuda_device, qwen, B, routing):
     assert moe.device_error(cuda_device) == 0
 
 
-def test_deepseek_sampled_tokens(cuda_device):
-    cfg = inputs.DEEPSEEK_V3
-    W = inputs.layer_weights(cfg, cuda_device)
-    Wd = device_mx(W, cuda_device)
-    for B in (1, 8, 32, 64):
-        x, ids, w = inputs.layer_batch(cfg, B)
-        compare_tokens(cuda_device, W, Wd, x, ids, w, [B - 1], f"deepseek B={B}")
-    del W, Wd
+@pytest.fixture(scope="module")
+def deepseek(cuda_device):
+    W = inputs.layer_weights(inputs.DEEPSEEK_V3, cuda_device)
+    yield W, device_mx(W, cuda_device)
+    del W
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("B", [1, 8])
+def test_deepseek_every_token(cuda_device, deepseek, B):
+    W, Wd = deepseek
+    x, ids, w = inputs.layer_batch(inputs.DEEPSEEK_V3, B)
+    compare_tokens(cuda_device, W, Wd, x, ids, w, range(B), f"deepseek B={B}", plain=False)
+
+
+@pytest.mark.parametrize("B", [32, 64])
+def test_deepseek_item_cover(cuda_device, deepseek, B):
+    """One token of every (expert, 4-token group) item, the shared expert's
+    groups included."""
+    W, Wd = deepseek
+    x, ids, w = inputs.layer_batch(inputs.DEEPSEEK_V3, B)
+    toks = item_cover(ids.numpy(), True)
+    compare_tokens(cuda_device, W, Wd, x, ids, w, toks, f"deepseek B={B} item cover", plain=False)
 
 
 # (E, k, d, I, shared): lanes-per-row L = 1, 2, 4, 8, 16, 32 on both passes,
@@ -148,10 +169,12 @@ def test_outputs_stay_in_bounds_edge(cuda_device, E, k, d, I, shared):
         compare_tokens(cuda_device, W, Wd, x, ids, w, range(B), f"canary {E},{k},{d},{I},{shared} B={B}")
 
 
-def test_hot_expert_and_duplicates(cuda_device):
+@pytest.mark.parametrize("d,I", [(128, 64), (256, 256)])
+def test_hot_expert_and_duplicates(cuda_device, d, I):
     """Every token on one expert (more tokens than one pass serves) and the
-    same expert twice inside one token's top-k (summed independently)."""
-    E, d, I = 4, 128, 64
+    same expert twice inside one token's top-k (summed independently); at
+    I = 256 the down pass is the row-tile kernel."""
+    E = 4
     W = small_weights(E, d, I, True, 2)
     Wd = device_mx(W, cuda_device)
     B, k = 13, 3
@@ -200,9 +223,12 @@ def test_bad_expert_id_sets_flag_and_skips_slot(cuda_device, tiny):
     assert moe.device_error(cuda_device) == 0
 
 
-def test_separate_passes_equal_layer(cuda_device, qwen):
+@pytest.mark.parametrize("B", [8, 32])
+def test_separate_passes_equal_layer(cuda_device, qwen, B):
+    """moe_layer (FP32 intermediate in the down pass's order) and the two
+    passes through the interface (BF16 h) give the same bits."""
     W, Wd = qwen
-    x, ids, w = inputs.layer_batch(inputs.QWEN3, 8)
+    x, ids, w = inputs.layer_batch(inputs.QWEN3, B)
     dev = cuda_device
     y1 = run_layer(dev, Wd, x, ids, w)
     h = run_gate_up(dev, Wd, x, ids)
