@@ -190,6 +190,42 @@ int moe_layer_host(const void* x_host, int B, int d, const int32_t* topk_ids_hos
                    size_t workspace_bytes, void* y_host, moe_stream_t stream);
 
 /*
+ * moe_layer_grouped -- the same layer computed expert-centrically, the way
+ * prefill and large batches are served [WD, section "Warp decode 與 Composer
+ * 訓練": expert-centric packing stays the right choice there; AS: the sorted
+ * blocks feed grouped GEMMs].  Steps, all on `stream`:
+ *   1. moe_align_block_size with block_size 128 (into the workspace);
+ *   2. if act_mx, x is rounded through MXFP8 (moe_mx_requant) first;
+ *   3. per block of 128 sorted slots and expert e:
+ *        g, u = the slots' x rows times deq(Wg[e]), deq(Wu[e]) (tensor
+ *        cores, BF16 operands -- exact for MXFP8 values -- FP32 sums),
+ *        h = bf16_rn( g * sigmoid(g) * u )  per slot;
+ *   4. if act_mx, h is rounded through MXFP8;
+ *   5. out[slot] = h[slot] times deq(Wd[e]) (FP32);
+ *   6. y[t,o] = bf16_rn( sum_j topk_w[t,j] * out[t*k+j, o] ), j in order.
+ * The sums run in the tensor cores' order, not the decode layer's, so the
+ * results agree with moe_layer to FP32 rounding, not bit for bit.  No shared
+ * expert.
+ * Arguments
+ *   x         BF16 [T][d], 32-byte aligned.  topk_ids int32 [T][k]; an id
+ *             outside [0, E) adds nothing and sets MOE_DEVERR_EXPERT_ID.
+ *   topk_w    float32 [T][k].  weights as for moe_layer; each scale array
+ *             4-byte aligned.
+ *   d, I      multiples of 128.  E <= MOE_ALIGN_MAX_EXPERTS; T*k +
+ *             E*127 < 2^31.  No limit on T beyond that.
+ *   act_mx    0: activations as given (the decode layer's numerics);
+ *             1: x and h rounded through MXFP8, the conventional path.
+ *   workspace >= moe_layer_grouped_workspace_bytes(), 256-byte aligned.
+ *   y         BF16 [T][d].
+ * Errors: MOE_ERR_SHAPE (d or I not a multiple of 128, k > E),
+ * MOE_ERR_LIMIT, MOE_ERR_WORKSPACE, MOE_ERR_ALIGN, MOE_ERR_CUDA.
+ */
+int moe_layer_grouped_workspace_bytes(int T, int k, int E, int d, int I, size_t* bytes);
+int moe_layer_grouped(const void* x, int T, int d, const int32_t* topk_ids, const float* topk_w, int k,
+                      moe_mx_t w_gate, moe_mx_t w_up, moe_mx_t w_down, int E, int I, int act_mx,
+                      void* workspace, size_t workspace_bytes, void* y, moe_stream_t stream);
+
+/*
  * moe_align_sizes -- output and workspace sizes for moe_align_block_size:
  *   n_sorted = T*k + E*(block_size-1)  (every expert's run padded at worst)
  *   n_blocks = ceil(n_sorted / block_size)

@@ -25,6 +25,7 @@ EXPORTS = ("moe_version", "moe_strerror", "moe_gate_up", "moe_down", "moe_layer_
            "moe_layer", "moe_layer_host_workspace_bytes", "moe_layer_host", "moe_align_sizes",
            "moe_align_block_size", "moe_align_block_size_static", "moe_align_static_fits",
            "moe_copy", "moe_device_error", "moe_router_topk", "moe_mx_requant", "moe_gate_up_fp4",
+           "moe_layer_grouped_workspace_bytes", "moe_layer_grouped",
            "moe_down_fp4")
 
 
@@ -78,6 +79,8 @@ def load(path: str = LIB_PATH):
         "moe_align_static_fits": ([I, I, I], I),
         "moe_copy": ([P, P, S, P], I),
         "moe_device_error": ([P, ctypes.POINTER(I)], I),
+        "moe_layer_grouped_workspace_bytes": ([I, I, I, I, I, ctypes.POINTER(S)], I),
+        "moe_layer_grouped": ([P, I, I, P, P, I, MXView, MXView, MXView, I, I, I, P, S, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -224,6 +227,40 @@ def layer(x, topk_ids, topk_w, w_gate: MX, w_up: MX, w_down: MX, shared=None,
                                       vg, vu, vd, E, I, _ref(vsg), _ref(vsu), _ref(vsd),
                                       workspace.data_ptr(), workspace.numel(), y.data_ptr(),
                                       _stream(dev)))
+    return y
+
+
+def layer_grouped_workspace_bytes(T: int, k: int, E: int, d: int, I: int) -> int:
+    out = ctypes.c_size_t()
+    _check("moe_layer_grouped_workspace_bytes",
+           load().moe_layer_grouped_workspace_bytes(T, k, E, d, I, ctypes.byref(out)))
+    return out.value
+
+
+def layer_grouped(x, topk_ids, topk_w, w_gate: MX, w_up: MX, w_down: MX, act_mx: bool = False,
+                  workspace: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None):
+    """The layer computed expert-centrically (align, grouped tensor-core GEMMs,
+    combine) on the current stream; act_mx rounds x and h through MXFP8."""
+    lib = load()
+    dev = x.device
+    _need(x, "x", torch.bfloat16, None, 2)
+    _need(topk_ids, "topk_ids", torch.int32, dev, 2)
+    _need(topk_w, "topk_w", torch.float32, dev, 2)
+    T, d = x.shape
+    k = topk_ids.shape[1]
+    E, I = w_gate.w.shape[0], w_gate.w.shape[1]
+    vg, vu = _mx(w_gate, "w_gate", dev, I, d), _mx(w_up, "w_up", dev, I, d, E)
+    vd = _mx(w_down, "w_down", dev, d, I, E)
+    need = layer_grouped_workspace_bytes(T, k, E, d, I)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    if y is None:
+        y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    _need(y, "y", torch.bfloat16, dev)
+    _check("moe_layer_grouped", lib.moe_layer_grouped(
+        x.data_ptr(), T, d, topk_ids.data_ptr(), topk_w.data_ptr(), k, vg, vu, vd, E, I, int(bool(act_mx)),
+        workspace.data_ptr(), workspace.numel(), y.data_ptr(), _stream(dev)))
     return y
 
 

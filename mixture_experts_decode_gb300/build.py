@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libmoedec.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["api.cu", "gate_up.cu", "down.cu", "align.cu", "router.cu", "requant.cu", "decode_fp4.cu"]
+SOURCES = ["api.cu", "gate_up.cu", "down.cu", "grouped.cu", "align.cu", "router.cu", "requant.cu", "decode_fp4.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
               "-I" + INCLUDE, "-I" + CSRC]
@@ -55,7 +55,9 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), lib_path: 
         with open(stamp) as f:
             if f.read().strip() == want:
                 return lib_path
-    obj_dir = os.path.join(BUILD_DIR, want[:12])
+    # one object folder per output library (rebuilt in place: the stamp, not
+    # the folder, records which sources it holds)
+    obj_dir = os.path.join(BUILD_DIR, os.path.basename(lib_path) + ".objs")
     os.makedirs(obj_dir, exist_ok=True)
     nvcc = _nvcc()
 

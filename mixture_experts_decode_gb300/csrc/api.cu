@@ -136,6 +136,48 @@ int down_checked(const void* h, bool h32, int B, int k, const int32_t* ids, cons
     return cuda_status(launch_down(s, h, h32, ids, w, view(&wd), view(sd), y, st, pdl));
 }
 
+// Carves the grouped layer's buffers out of one workspace (256-byte aligned
+// pieces); returns the bytes used.  ws == nullptr only measures.
+size_t grouped_carve(int T, int k, int E, int d, int I, char* base, GroupedWorkspace* ws) {
+    const int64_t ns = (int64_t)T * k + (int64_t)E * (GROUPED_BLOCK - 1);
+    const int64_t nb = (ns + GROUPED_BLOCK - 1) / GROUPED_BLOCK;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        char* p = base ? base + off : nullptr;
+        off += round_up(bytes, 256);
+        return p;
+    };
+    char* sorted = take((size_t)ns * 4);
+    char* eids = take((size_t)nb * 4);
+    char* ntpp = take(4);
+    char* aws = take(align_workspace_bytes((int64_t)T * k, E));
+    char* xmx = take((size_t)T * d * 2);
+    char* hs = take((size_t)ns * I * 2);
+    char* out = take((size_t)T * k * d * 4);
+    if (ws) {
+        ws->sorted = reinterpret_cast<int32_t*>(sorted);
+        ws->n_sorted = ns;
+        ws->expert_ids = reinterpret_cast<int32_t*>(eids);
+        ws->n_blocks = nb;
+        ws->ntpp = reinterpret_cast<int32_t*>(ntpp);
+        ws->align_ws = aws;
+        ws->x_mx = reinterpret_cast<uint16_t*>(xmx);
+        ws->h_sorted = reinterpret_cast<uint16_t*>(hs);
+        ws->out = reinterpret_cast<float*>(out);
+    }
+    return off;
+}
+
+int check_grouped_shape(int T, int k, int E, int d, int I) {
+    if (T < 0 || k < 0 || E < 0 || d < 0 || I < 0) return MOE_ERR_ARG;
+    if (d == 0 || I == 0 || E == 0 || k == 0 || k > E) return MOE_ERR_SHAPE;
+    if (!grouped_shape_ok(d, I)) return MOE_ERR_SHAPE;
+    if (E > MOE_ALIGN_MAX_EXPERTS) return MOE_ERR_LIMIT;
+    const int64_t ns = (int64_t)T * k + (int64_t)E * (GROUPED_BLOCK - 1);
+    if (ns > 0x7fffffffLL || (int64_t)T * k * d > ((int64_t)1 << 40)) return MOE_ERR_LIMIT;
+    return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -283,6 +325,39 @@ int moe_layer_host(const void* x_host, int B, int d, const int32_t* topk_ids_hos
     if (cudaMemcpyAsync(y_host, yd, (size_t)B * d * 2, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
+}
+
+int moe_layer_grouped_workspace_bytes(int T, int k, int E, int d, int I, size_t* bytes) {
+    if (!bytes) return MOE_ERR_ARG;
+    const int rc = check_grouped_shape(T, k, E, d, I);
+    if (rc) return rc;
+    *bytes = grouped_carve(T, k, E, d, I, nullptr, nullptr);
+    return MOE_OK;
+}
+
+int moe_layer_grouped(const void* x, int T, int d, const int32_t* topk_ids, const float* topk_w, int k,
+                      moe_mx_t w_gate, moe_mx_t w_up, moe_mx_t w_down, int E, int I, int act_mx,
+                      void* workspace, size_t workspace_bytes, void* y, moe_stream_t stream) {
+    int rc = check_grouped_shape(T, k, E, d, I);
+    if (rc) return rc;
+    if (act_mx != 0 && act_mx != 1) return MOE_ERR_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !topk_ids || !topk_w || !y) return MOE_ERR_ARG;
+    if ((rc = check_mx(w_gate)) || (rc = check_mx(w_up)) || (rc = check_mx(w_down))) return rc;
+    if (!aligned(w_gate.s, 4) || !aligned(w_up.s, 4) || !aligned(w_down.s, 4)) return MOE_ERR_ALIGN;
+    if (!aligned(x, 32) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(y, 2)) return MOE_ERR_ALIGN;
+    const size_t need = grouped_carve(T, k, E, d, I, nullptr, nullptr);
+    if (!workspace || workspace_bytes < need) return MOE_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return MOE_ERR_ALIGN;
+    DeviceInfo di;
+    if (device_info(&di) != cudaSuccess) return MOE_ERR_CUDA;
+    if (align_smem_bytes(E) > (size_t)di.max_smem_optin || grouped_smem_bytes(d, I) > (size_t)di.max_smem_optin)
+        return MOE_ERR_LIMIT;
+    GroupedWorkspace ws{};
+    grouped_carve(T, k, E, d, I, static_cast<char*>(workspace), &ws);
+    return cuda_status(launch_grouped(static_cast<const uint16_t*>(x), T, d, topk_ids, topk_w, k, view(&w_gate),
+                                      view(&w_up), view(&w_down), E, I, act_mx != 0, ws,
+                                      static_cast<uint16_t*>(y), (cudaStream_t)stream));
 }
 
 int moe_router_topk(const float* logits, int B, int E, int k, int score, float scale, int32_t* topk_ids,

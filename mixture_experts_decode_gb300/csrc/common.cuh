@@ -70,6 +70,26 @@ __device__ __forceinline__ void e4m3x4_to_float(uint32_t w, float2& lo, float2& 
     hi = __half22float2(hb);
 }
 
+// One 32-bit word of codes (four bytes, each an E2M1 pair with the lower K
+// index in the low nibble) -> four float2 (x = lower K index), exact.
+__device__ __forceinline__ void e2m1x8_to_float(uint32_t w, float2 (&f)[4]) {
+    uint32_t h[4];
+    asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3; }"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 hh;
+        memcpy(&hh, &h[i], 4);
+        f[i] = __half22float2(hh);
+    }
+}
+
 // E8M0 scale byte -> 2^(s-127) as float (s = 0 gives the subnormal 2^-127;
 // s = 255, NaN in the format, is a precondition violation and yields inf).
 __device__ __forceinline__ float e8m0_to_float(uint32_t s) {
@@ -116,21 +136,6 @@ __device__ __forceinline__ void cp_async_16(void* smem, const void* gmem, int sr
 __device__ __forceinline__ void cp_async_4(void* smem, const void* gmem, int src_bytes) {
     const uint32_t a = (uint32_t)__cvta_generic_to_shared(smem);
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(a), "l"(gmem), "r"(src_bytes) : "memory");
-}
-
-// 8 bytes by cp.async (the .ca form, the only one for 8-byte copies; both
-// addresses 8-byte aligned).
-__device__ __forceinline__ void cp_async_8(void* smem, const void* gmem) {
-    const uint32_t a = (uint32_t)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(a), "l"(gmem) : "memory");
-}
-
-// One arrival on `bar` once every cp.async this thread issued so far has
-// landed; the barrier's expected count must include it (.noinc).
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
-                     (uint32_t)__cvta_generic_to_shared(bar))
-                 : "memory");
 }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }

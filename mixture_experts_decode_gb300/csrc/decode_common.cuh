@@ -43,14 +43,13 @@ struct DownArgs {
 };
 
 // Position of intermediate neuron n inside a row of the FP32 intermediate
-// that the gate/up pass writes for the row-tile down pass (I % 256 == 0):
-// each 256-element slab is stored as [8 groups of 4][8 lanes][4], so lane
-// kr of that pass, which owns elements kr*32 .. kr*32+31 of the slab, finds
-// its group q at float4 index q*8 + kr and the eight lanes' loads of one q
-// cover 128 consecutive bytes.
+// that the gate/up pass writes for the down pass (I % 256 == 0).  The down
+// pass's lane l takes elements 8 l .. 8 l + 7 of each 256-element group;
+// the group is stored as [2 halves][32 lanes][4], so that lane's two
+// 16-byte loads are contiguous across the warp (bank-conflict free).
 __host__ __device__ inline int h32_pos(int n) {
-    const int w = n & 255;
-    return (n & ~255) | ((((w >> 2) & 7) * 8 + (w >> 5)) << 2) | (w & 3);
+    const int w = n & 255, l = w >> 3, e = w & 7;
+    return (n & ~255) | ((e >> 2) << 7) | (l << 2) | (e & 3);
 }
 
 // Store one intermediate value: BF16 round to nearest even, then either the

@@ -4,8 +4,12 @@
 // MoE operators).  Activations BF16, products and sums FP32, h BF16, y BF16,
 // exactly as for the MXFP8 weights.
 //
-// A first FP4 path, organised as the "Warp decode" page describes its two
-// kernels (section "兩個 kernel 的運作方式"): one warp per output value.
+// This file holds the fallback FP4 kernels, organised as the "Warp decode"
+// page describes its two kernels (section "兩個 kernel 的運作方式"): one warp
+// per output value.  Shapes that the grouped kernels take (gate_up.cu,
+// down.cu: d % 512 == 0 and I % 16 == 0 for gate/up with B >= 2, I % 256 ==
+// 0 for down, 16-byte aligned weights) run there instead, streaming each
+// distinct expert's rows once per call.
 //   gate/up: a warp owns one (token, slot, neuron) and streams the gate and
 //     up rows of the slot's expert once; lanes take 16-byte chunks (32 codes
 //     = one scale block) and the matching 32 values of x, loaded for each
@@ -35,26 +39,6 @@ __device__ __forceinline__ uint4 ld_nc_128(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
-}
-
-// One 32-bit word of codes (four bytes, each an E2M1 pair with the lower K
-// index in the low nibble) -> four float2 (x = lower K index), exact.
-__device__ __forceinline__ void e2m1x8_to_float(uint32_t w, float2 (&f)[4]) {
-    uint32_t h[4];
-    asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
-        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %3, b3; }"
-        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-        : "r"(w));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        __half2 hh;
-        memcpy(&hh, &h[i], 4);
-        f[i] = __half22float2(hh);
-    }
 }
 
 // Partial dot of one 32-element chunk: 16 code bytes against 32 BF16 values.
@@ -159,11 +143,17 @@ __global__ void __launch_bounds__(F4_WARPS * 32) down_fp4_kernel(F4Args a) {
         const uint8_t* wdr = vd.w + row * (s.I / 2);
         const uint8_t* sdr = vd.s + row * (s.I / 32);
         const uint16_t* hr = a.h + ((int64_t)b * KS + j) * s.I;
+        // the block scale multiplies each chunk's partial sum (exact, a power
+        // of two, while the product stays in FP32's normal range); the
+        // routing weight multiplies the expert's whole dot once, as the
+        // grouped kernels do
+        float2 ex = make_float2(0.f, 0.f);
         for (int c = lane; c < s.I / 32; c += 32) {
             const uint4 w4 = ld_nc_128(wdr + c * 16);
-            const float sw = e8m0_to_float(ld_stream_u8(sdr + c)) * wt;  // exact: a power of two times wt
-            acc = __ffma2_rn(chunk_dot(w4, hr + c * 32), make_float2(sw, sw), acc);
+            const float sc = e8m0_to_float(ld_stream_u8(sdr + c));
+            ex = __ffma2_rn(chunk_dot(w4, hr + c * 32), make_float2(sc, sc), ex);
         }
+        acc = __ffma2_rn(ex, make_float2(wt, wt), acc);
     }
     const float v = warp_sum(acc.x + acc.y);
     if (lane == 0) a.out[(int64_t)b * s.d + o] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
@@ -179,8 +169,11 @@ static cudaError_t launch_fp4(void (*kernel)(F4Args), const F4Args& a, int64_t i
 
 cudaError_t launch_gate_up_fp4(const DecodeShape& s, const void* x, const int32_t* ids, MXView wg, MXView wu,
                                MXView shg, MXView shu, void* h, cudaStream_t st) {
+    cudaError_t err = cudaSuccess;
+    // the grouped kernel (each distinct expert's rows streamed once) when it applies
+    if (launch_gate_up_grouped_fp4(s, x, ids, wg, wu, shg, shu, h, st, &err)) return err;
     DeviceInfo di;
-    cudaError_t err = device_info(&di);
+    err = device_info(&di);
     if (err != cudaSuccess) return err;
     F4Args a{};
     a.s = s;
@@ -197,8 +190,10 @@ cudaError_t launch_gate_up_fp4(const DecodeShape& s, const void* x, const int32_
 
 cudaError_t launch_down_fp4(const DecodeShape& s, const void* h, const int32_t* ids, const float* w, MXView wd,
                             MXView shd, void* y, cudaStream_t st) {
+    cudaError_t err = cudaSuccess;
+    if (launch_down_grouped_fp4(s, h, ids, w, wd, shd, y, st, &err)) return err;
     DeviceInfo di;
-    cudaError_t err = device_info(&di);
+    err = device_info(&di);
     if (err != cudaSuccess) return err;
     F4Args a{};
     a.s = s;

@@ -566,9 +566,12 @@ constexpr int GU4_KT = 512;   // K elements per stage (16 scale blocks)
 constexpr int GU4_BOX = 128;  // inner box of a weight tensor copy (bytes)
 constexpr int GU4_S = 4;      // ring stages
 
-template <int RT>
+// FP4: MXFP4 weights, two E2M1 codes per byte, so a stage's code bytes
+// per row are half those of MXFP8.
+template <int RT, bool FP4 = false>
 struct __align__(1024) GU4Stage {
-    uint8_t w[2][GU4_KT / GU4_BOX][RT][GU4_BOX];  // [proj][box][row][128 B, swizzled]
+    static constexpr int BOXES = GU4_KT / (FP4 ? 2 : 1) / GU4_BOX;
+    uint8_t w[2][BOXES][RT][GU4_BOX];             // [proj][box][row][128 B, swizzled]
     uint8_t sc[2][RT][GU4_KT / 32];               // [proj][row][block] E8M0
     uint16_t x[TC][GU4_KT];                       // BF16 activations of the slice
 };
@@ -596,8 +599,8 @@ struct GU4Maps {
 };
 __host__ __device__ inline size_t gu4_ring_offset(const DecodeShape& s) { return map_ints(s, false) * 4; }
 
-template <int RT, int CW, int NT>
-__device__ __forceinline__ void gu4_group(const GateUpArgs& a, GU4Stage<RT>* ring, GU4Shared<RT, CW>* sh,
+template <int RT, int CW, int NT, bool FP4>
+__device__ __forceinline__ void gu4_group(const GateUpArgs& a, GU4Stage<RT, FP4>* ring, GU4Shared<RT, CW>* sh,
                                           RingPos& rp, int grp, int nkt, int warp, int lane, int n0,
                                           const int* hs) {
     constexpr int LPR = 32 / RT;       // lanes per row
@@ -617,7 +620,7 @@ __device__ __forceinline__ void gu4_group(const GateUpArgs& a, GU4Stage<RT>* rin
     for (int kt = 0; kt < nkt; ++kt, rp.next(GU4_S)) {
         const int slot = rp.slot;
         if (!mbar_wait_abort(&sh->full[slot], rp.par, &sh->abort)) continue;
-        const GU4Stage<RT>& st = ring[slot];
+        const GU4Stage<RT, FP4>& st = ring[slot];
         {  // this warp's blocks of x -> FP32: lane = (token, four K elements of each block)
             const int t = lane >> 3, k = (lane & 7) * 4;
             if (t < NT) {
@@ -634,27 +637,56 @@ __device__ __forceinline__ void gu4_group(const GateUpArgs& a, GU4Stage<RT>* rin
         __syncwarp();
         const float* xl = xf + hb * GU4_XH;
         float2 part[2][NT];
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {  // two 16-byte chunks = this lane's 32 K elements
+        if constexpr (FP4) {
+            // one 16-byte chunk holds the lane's whole 32-element block
             uint4 wv[2];
 #pragma unroll
             for (int p = 0; p < 2; ++p)
-                wv[p] = *reinterpret_cast<const uint4*>(&st.w[p][box][r][((c0 + c2) ^ sw) * 16]);
+                wv[p] = *reinterpret_cast<const uint4*>(&st.w[p][blk >> 3][r][((blk & 7) ^ sw) * 16]);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float2 wq[2][2];
+            for (int q8 = 0; q8 < 4; ++q8) {  // eight K elements per code word
+                float2 wq[2][4];
 #pragma unroll
-                for (int p = 0; p < 2; ++p) e4m3x4_to_float((&wv[p].x)[q4], wq[p][0], wq[p][1]);
+                for (int p = 0; p < 2; ++p) e2m1x8_to_float((&wv[p].x)[q8], wq[p]);
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
-                    const float4 xv = *reinterpret_cast<const float4*>(xl + t * XS + c2 * 16 + q4 * 4);
+                    const float4 x0 = *reinterpret_cast<const float4*>(xl + t * XS + q8 * 8);
+                    const float4 x1 = *reinterpret_cast<const float4*>(xl + t * XS + q8 * 8 + 4);
 #pragma unroll
                     for (int p = 0; p < 2; ++p) {
-                        if (c2 == 0 && q4 == 0)
-                            part[p][t] = __fmul2_rn(make_float2(xv.x, xv.y), wq[p][0]);
+                        if (q8 == 0)
+                            part[p][t] = __fmul2_rn(make_float2(x0.x, x0.y), wq[p][0]);
                         else
-                            part[p][t] = __ffma2_rn(make_float2(xv.x, xv.y), wq[p][0], part[p][t]);
-                        part[p][t] = __ffma2_rn(make_float2(xv.z, xv.w), wq[p][1], part[p][t]);
+                            part[p][t] = __ffma2_rn(make_float2(x0.x, x0.y), wq[p][0], part[p][t]);
+                        part[p][t] = __ffma2_rn(make_float2(x0.z, x0.w), wq[p][1], part[p][t]);
+                        part[p][t] = __ffma2_rn(make_float2(x1.x, x1.y), wq[p][2], part[p][t]);
+                        part[p][t] = __ffma2_rn(make_float2(x1.z, x1.w), wq[p][3], part[p][t]);
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {  // two 16-byte chunks = this lane's 32 K elements
+                uint4 wv[2];
+#pragma unroll
+                for (int p = 0; p < 2; ++p)
+                    wv[p] = *reinterpret_cast<const uint4*>(&st.w[p][box][r][((c0 + c2) ^ sw) * 16]);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    float2 wq[2][2];
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) e4m3x4_to_float((&wv[p].x)[q4], wq[p][0], wq[p][1]);
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        const float4 xv = *reinterpret_cast<const float4*>(xl + t * XS + c2 * 16 + q4 * 4);
+#pragma unroll
+                        for (int p = 0; p < 2; ++p) {
+                            if (c2 == 0 && q4 == 0)
+                                part[p][t] = __fmul2_rn(make_float2(xv.x, xv.y), wq[p][0]);
+                            else
+                                part[p][t] = __ffma2_rn(make_float2(xv.x, xv.y), wq[p][0], part[p][t]);
+                            part[p][t] = __ffma2_rn(make_float2(xv.z, xv.w), wq[p][1], part[p][t]);
+                        }
                     }
                 }
             }
@@ -705,7 +737,7 @@ __device__ __forceinline__ void gu4_group(const GateUpArgs& a, GU4Stage<RT>* rin
     }
 }
 
-template <int RT, int CW>
+template <int RT, int CW, bool FP4>
 __global__ void __launch_bounds__((CW + 1) * 32, RT == 32 ? 1 : 2)
     gate_up_v4_kernel(GateUpArgs a, const __grid_constant__ GU4Maps maps) {
     constexpr int S = GU4_S;
@@ -715,7 +747,8 @@ __global__ void __launch_bounds__((CW + 1) * 32, RT == 32 ? 1 : 2)
     // swizzled tensor copies want 1024-byte aligned boxes: align at run time
     // (the launch reserves 1024 spare bytes)
     const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_i) + gu4_ring_offset(s);
-    GU4Stage<RT>* ring = reinterpret_cast<GU4Stage<RT>*>((raw + 1023) & ~uintptr_t(1023));
+    using Stage = GU4Stage<RT, FP4>;
+    Stage* ring = reinterpret_cast<Stage*>((raw + 1023) & ~uintptr_t(1023));
     GU4Shared<RT, CW>* sh = reinterpret_cast<GU4Shared<RT, CW>*>(ring + S);
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
@@ -727,7 +760,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, RT == 32 ? 1 : 2)
     }
     // the copy ring is idle until the map is built: it serves as the map's scratch
     build_route_map(m, a.ids, nullptr, s, a.err, false, reinterpret_cast<int*>(ring),
-                    (int)(S * sizeof(GU4Stage<RT>) / 4));  // ends with __syncthreads
+                    (int)(S * sizeof(Stage) / 4));  // ends with __syncthreads
     asm volatile("griddepcontrol.launch_dependents;");
 
     const int nu = m.hdr[0];
@@ -770,19 +803,20 @@ __global__ void __launch_bounds__((CW + 1) * 32, RT == 32 ? 1 : 2)
                         ok = false;
                         break;
                     }
-                    GU4Stage<RT>& st = ring[slot];
+                    Stage& st = ring[slot];
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(&sh->full[slot], 2 * RT * (GU4_KT + GU4_KT / 32) + nt * GU4_KT * 2);
+                        mbar_arrive_expect_tx(&sh->full[slot], 2 * RT * (Stage::BOXES * GU4_BOX + GU4_KT / 32) +
+                                                                   nt * GU4_KT * 2);
                         fence_proxy_async();
 #pragma unroll
                         for (int p = 0; p < 2; ++p) {
                             if (maps.w3d) {
-                                tma_3d(st.w[p][0], &maps.w[shx][p], 0, row0, kt * (GU4_KT / GU4_BOX), &sh->full[slot],
+                                tma_3d(st.w[p][0], &maps.w[shx][p], 0, row0, kt * Stage::BOXES, &sh->full[slot],
                                        pol);
                             } else {
 #pragma unroll
-                                for (int b = 0; b < GU4_KT / GU4_BOX; ++b)
-                                    tma_2d(st.w[p][b], &maps.w[shx][p], kt * GU4_KT + b * GU4_BOX, row0,
+                                for (int b = 0; b < Stage::BOXES; ++b)
+                                    tma_2d(st.w[p][b], &maps.w[shx][p], (kt * Stage::BOXES + b) * GU4_BOX, row0,
                                            &sh->full[slot], pol);
                             }
                             tma_2d(st.sc[p], &maps.s[shx][p], kt * (GU4_KT / 32), row0, &sh->full[slot], pol);
@@ -813,10 +847,10 @@ __global__ void __launch_bounds__((CW + 1) * 32, RT == 32 ? 1 : 2)
                 const int nt = min(TC, s1 - t0);
                 const int* hs = m.hrow + t0;
                 switch (nt) {
-                    case 1: gu4_group<RT, CW, 1>(a, ring, sh, rp, grp, nkt, warp, lane, n0, hs); break;
-                    case 2: gu4_group<RT, CW, 2>(a, ring, sh, rp, grp, nkt, warp, lane, n0, hs); break;
-                    case 3: gu4_group<RT, CW, 3>(a, ring, sh, rp, grp, nkt, warp, lane, n0, hs); break;
-                    default: gu4_group<RT, CW, 4>(a, ring, sh, rp, grp, nkt, warp, lane, n0, hs); break;
+                    case 1: gu4_group<RT, CW, 1, FP4>(a, ring, sh, rp, grp, nkt, warp, lane, n0, hs); break;
+                    case 2: gu4_group<RT, CW, 2, FP4>(a, ring, sh, rp, grp, nkt, warp, lane, n0, hs); break;
+                    case 3: gu4_group<RT, CW, 3, FP4>(a, ring, sh, rp, grp, nkt, warp, lane, n0, hs); break;
+                    default: gu4_group<RT, CW, 4, FP4>(a, ring, sh, rp, grp, nkt, warp, lane, n0, hs); break;
                 }
             }
         }
@@ -926,21 +960,23 @@ constexpr int GU4_HOST_CW = 8;
 
 static bool gate_up_v4_ok(const GateUpArgs& a) {
     const DecodeShape& s = a.s;
-    if (s.d % GU4_KT || s.I % GU4_HOST_RT) return false;
+    if (s.d % GU4_KT || s.I % GU4_HOST_RT) return false;  // (MXFP4: 256-byte code stages, 128-byte boxes)
     if (!aligned16(a.wg.w) || !aligned16(a.wu.w) || !aligned16(a.wg.s) || !aligned16(a.wu.s)) return false;
     if (s.S && (!aligned16(a.shg.w) || !aligned16(a.shu.w) || !aligned16(a.shg.s) || !aligned16(a.shu.s)))
         return false;
     return true;
 }
 
-static size_t gate_up_v4_smem(const DecodeShape& s) {
-    return gu4_ring_offset(s) + 1024 + (size_t)GU4_S * sizeof(GU4Stage<GU4_HOST_RT>) +
-           sizeof(GU4Shared<GU4_HOST_RT, GU4_HOST_CW>);
+static size_t gate_up_v4_smem(const DecodeShape& s, bool fp4) {
+    const size_t stage = fp4 ? sizeof(GU4Stage<GU4_HOST_RT, true>) : sizeof(GU4Stage<GU4_HOST_RT, false>);
+    return gu4_ring_offset(s) + 1024 + (size_t)GU4_S * stage + sizeof(GU4Shared<GU4_HOST_RT, GU4_HOST_CW>);
 }
 
 
-static bool gate_up_v4_maps(const GateUpArgs& a, GU4Maps* maps) {
+static bool gate_up_v4_maps(const GateUpArgs& a, bool fp4, GU4Maps* maps) {
     const DecodeShape& s = a.s;
+    const uint64_t cols = fp4 ? s.d / 2 : s.d;  // code bytes per row
+    const uint32_t nblk = (uint32_t)(GU4_KT / (fp4 ? 2 : 1) / GU4_BOX);
     const MXView v[2][2] = {{a.wg, a.wu}, {a.shg, a.shu}};
     // one 3D copy per projection and stage when the driver takes the block
     // view, else four 2D copies
@@ -951,8 +987,8 @@ static bool gate_up_v4_maps(const GateUpArgs& a, GU4Maps* maps) {
             for (int p = 0; p < 2 && ok; ++p) {
                 const MXView& m = sh && !s.S ? v[0][p] : v[sh][p];  // no shared expert: any valid map
                 const uint64_t r = (uint64_t)(sh && s.S ? 1 : s.E) * s.I;
-                ok = maps->w3d ? map_3d_u8_blocks(&maps->w[sh][p], m.w, r, s.d, GU4_HOST_RT, GU4_KT / GU4_BOX)
-                               : map_2d_u8(&maps->w[sh][p], m.w, r, s.d, GU4_HOST_RT, GU4_BOX, true);
+                ok = maps->w3d ? map_3d_u8_blocks(&maps->w[sh][p], m.w, r, cols, GU4_HOST_RT, nblk)
+                               : map_2d_u8(&maps->w[sh][p], m.w, r, cols, GU4_HOST_RT, GU4_BOX, true);
                 ok = ok && map_2d_u8(&maps->s[sh][p], m.s, r, s.d / 32, GU4_HOST_RT, GU4_KT / 32);
             }
         }
@@ -964,13 +1000,14 @@ static bool gate_up_v4_maps(const GateUpArgs& a, GU4Maps* maps) {
 }
 
 // Resident CTAs per SM (0 when the kernel cannot be resident).
-static int gate_up_v4_occupancy(size_t smem, int dev) {
+static int gate_up_v4_occupancy(size_t smem, int dev, bool fp4) {
     static std::mutex mu;
-    static int occ_cache[64] = {0};
-    static size_t smem_cache[64] = {0};
+    static int occ_cache[2][64] = {{0}};
+    static size_t smem_cache[2][64] = {{0}};
     std::lock_guard<std::mutex> lock(mu);
-    if (dev < 64 && smem_cache[dev] == smem) return occ_cache[dev];
-    auto* fn = gate_up_v4_kernel<GU4_HOST_RT, GU4_HOST_CW>;
+    if (dev < 0 || dev >= 64) return 0;
+    if (smem_cache[fp4][dev] == smem) return occ_cache[fp4][dev];
+    auto* fn = fp4 ? gate_up_v4_kernel<GU4_HOST_RT, GU4_HOST_CW, true> : gate_up_v4_kernel<GU4_HOST_RT, GU4_HOST_CW, false>;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
         cudaGetLastError();
         return 0;
@@ -980,21 +1017,42 @@ static int gate_up_v4_occupancy(size_t smem, int dev) {
         cudaGetLastError();
         bps = 0;
     }
-    if (dev < 64) {
-        occ_cache[dev] = bps;
-        smem_cache[dev] = smem;
-    }
+    occ_cache[fp4][dev] = bps;
+    smem_cache[fp4][dev] = smem;
     return bps;
 }
 
 static cudaError_t launch_gate_up_v4(const GateUpArgs& a, const GU4Maps& maps, size_t smem, int bps,
-                                     const DeviceInfo& di, cudaStream_t st) {
+                                     const DeviceInfo& di, cudaStream_t st, bool fp4) {
     const long tiles = (long)max_unique(a.s) * (a.s.I / GU4_HOST_RT);
     long grid = std::min<long>((long)di.sm_count * bps, tiles);
     if (grid < 1) grid = 1;
-    gate_up_v4_kernel<GU4_HOST_RT, GU4_HOST_CW><<<(unsigned)grid, (GU4_HOST_CW + 1) * 32, smem, st>>>(a, maps);
+    if (fp4)
+        gate_up_v4_kernel<GU4_HOST_RT, GU4_HOST_CW, true><<<(unsigned)grid, (GU4_HOST_CW + 1) * 32, smem, st>>>(a, maps);
+    else
+        gate_up_v4_kernel<GU4_HOST_RT, GU4_HOST_CW, false><<<(unsigned)grid, (GU4_HOST_CW + 1) * 32, smem, st>>>(a, maps);
     return cudaGetLastError();
 }
+
+// The grouped gate/up kernel with MXFP4 weights (moe_gate_up_fp4); returns
+// false when the shape or alignment does not suit it (the caller then uses
+// the one-warp-per-output kernel).
+bool launch_gate_up_grouped_fp4(const DecodeShape& s, const void* x, const int32_t* ids, MXView wg, MXView wu,
+                                MXView shg, MXView shu, void* h, cudaStream_t st, cudaError_t* err) {
+    DeviceInfo di;
+    if ((*err = device_info(&di)) != cudaSuccess) return true;
+    int dev = 0;
+    if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return true;
+    GateUpArgs a{s, (const uint16_t*)x, ids, wg, wu, shg, shu, (uint16_t*)h, di.err_word, nullptr};
+    if (s.B < 2 || !gate_up_v4_ok(a)) return false;
+    const size_t smem = gate_up_v4_smem(s, true);
+    const int bps = smem <= (size_t)di.max_smem_optin ? gate_up_v4_occupancy(smem, dev, true) : 0;
+    GU4Maps maps;
+    if (bps < 1 || !gate_up_v4_maps(a, true, &maps)) return false;
+    *err = launch_gate_up_v4(a, maps, smem, bps, di, st, true);
+    return true;
+}
+
 
 
 cudaError_t launch_gate_up(const DecodeShape& s, const void* x, const int32_t* ids, MXView wg,
@@ -1007,10 +1065,10 @@ cudaError_t launch_gate_up(const DecodeShape& s, const void* x, const int32_t* i
     GateUpArgs a{s, (const uint16_t*)x, ids, wg, wu, shg, shu, h32 ? nullptr : (uint16_t*)h, di.err_word,
                  h32 ? (float*)h : nullptr};
     if (s.B >= 2 && gate_up_v4_ok(a)) {
-        const size_t smem = gate_up_v4_smem(s);
+        const size_t smem = gate_up_v4_smem(s, false);
         GU4Maps maps;
-        const int bps = smem <= (size_t)di.max_smem_optin ? gate_up_v4_occupancy(smem, dev) : 0;
-        if (bps >= 1 && gate_up_v4_maps(a, &maps)) return launch_gate_up_v4(a, maps, smem, bps, di, st);
+        const int bps = smem <= (size_t)di.max_smem_optin ? gate_up_v4_occupancy(smem, dev, false) : 0;
+        if (bps >= 1 && gate_up_v4_maps(a, false, &maps)) return launch_gate_up_v4(a, maps, smem, bps, di, st, false);
     }
     if (gate_up_v3_ok(a) && gate_up_v3_smem(s) <= (size_t)di.max_smem_optin) {
         GU3Maps maps;

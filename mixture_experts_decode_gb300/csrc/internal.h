@@ -38,6 +38,13 @@ cudaError_t launch_router(const float* logits, int B, int E, int k, int score, f
 cudaError_t launch_mx_requant(const void* in, void* out, int64_t rows, int K, cudaStream_t st);
 cudaError_t launch_gate_up_fp4(const DecodeShape& s, const void* x, const int32_t* ids, MXView wg, MXView wu,
                                MXView shg, MXView shu, void* h, cudaStream_t st);
+// The grouped (one pass over each distinct expert's rows) kernels with MXFP4
+// weights: return false, launching nothing, when the shape or alignment
+// does not suit them; else launch and set *err.
+bool launch_gate_up_grouped_fp4(const DecodeShape& s, const void* x, const int32_t* ids, MXView wg, MXView wu,
+                                MXView shg, MXView shu, void* h, cudaStream_t st, cudaError_t* err);
+bool launch_down_grouped_fp4(const DecodeShape& s, const void* h, const int32_t* ids, const float* w, MXView wd,
+                             MXView shd, void* y, cudaStream_t st, cudaError_t* err);
 cudaError_t launch_down_fp4(const DecodeShape& s, const void* h, const int32_t* ids, const float* w, MXView wd,
                             MXView shd, void* y, cudaStream_t st);
 // Shared-memory bytes the decode kernels need; 0 if the shape is beyond the
@@ -54,5 +61,25 @@ size_t align_smem_bytes(int E);
 cudaError_t align_static_scratch(void** out);
 
 cudaError_t launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t st);
+
+// The expert-centric (grouped GEMM) layer's device buffers, carved from the
+// caller's workspace.
+struct GroupedWorkspace {
+    int32_t* sorted;      // [n_sorted] flat slot of each sorted row (T*k = pad)
+    int64_t n_sorted;
+    int32_t* expert_ids;  // [n_blocks]
+    int64_t n_blocks;
+    int32_t* ntpp;        // rows used, a multiple of the block size
+    void* align_ws;
+    uint16_t* x_mx;       // [T][d] x rounded through MXFP8 (act_mx only)
+    uint16_t* h_sorted;   // [n_sorted][I] BF16
+    float* out;           // [T*k][d] FP32 per-slot partial outputs
+};
+constexpr int GROUPED_BLOCK = 128;  // sorted rows per block (the MMA's M)
+bool grouped_shape_ok(int d, int I);
+size_t grouped_smem_bytes(int d, int I);
+cudaError_t launch_grouped(const uint16_t* x, int T, int d, const int32_t* ids, const float* w, int k, MXView wg,
+                           MXView wu, MXView wd, int E, int I, bool act_mx, const GroupedWorkspace& ws, uint16_t* y,
+                           cudaStream_t st);
 
 }  // namespace moedec

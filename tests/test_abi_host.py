@@ -136,3 +136,27 @@ def test_fp4_passes_reject_bad_arguments_before_launch(lib):
     assert lib.moe_down_fp4(h, 4, 2, ids, w, mx, 8, 64, 48, None, y, None) == -2                 # I % 32
     assert lib.moe_down_fp4(h, 4, 2, ids, None, mx, 8, 64, 64, None, y, None) == -1             # NULL
     assert lib.moe_down_fp4(P(0x500008), 4, 2, ids, w, mx, 8, 64, 64, None, y, None) == -5
+
+
+def test_grouped_layer_rejects_bad_arguments_before_launch(lib):
+    m = _mx()
+    ws = ctypes.c_size_t()
+    assert lib.moe_layer_grouped_workspace_bytes(256, 8, 128, 2048, 768, ctypes.byref(ws)) == 0
+    ns = 256 * 8 + 128 * 127
+    # at least the sort output, h for every sorted row and the FP32 per-slot outputs
+    assert ws.value >= ns * 4 + ns * 768 * 2 + 256 * 8 * 2048 * 4
+    assert lib.moe_layer_grouped_workspace_bytes(4, 2, 8, 96, 256, ctypes.byref(ws)) == -2   # d % 128
+    assert lib.moe_layer_grouped_workspace_bytes(4, 2, 8, 256, 160, ctypes.byref(ws)) == -2  # I % 128
+    assert lib.moe_layer_grouped_workspace_bytes(4, 9, 8, 256, 256, ctypes.byref(ws)) == -2   # k > E
+    assert lib.moe_layer_grouped_workspace_bytes(4, 2, 1025, 256, 256, ctypes.byref(ws)) == -3
+    assert lib.moe_layer_grouped_workspace_bytes(-1, 2, 8, 256, 256, ctypes.byref(ws)) == -1
+
+    def call(T=4, x=0x20000, ids=0x30000, w=0x40000, act=0, wsp=0x70000, wsb=1 << 40, y=0x60000):
+        return lib.moe_layer_grouped(x, T, 256, ids, w, 2, m, m, m, 8, 256, act, wsp, wsb, y, None)
+
+    assert call(act=2) == -1
+    assert call(x=0) == -1
+    assert call(x=0x20010) == -5                          # x not 32-byte aligned
+    assert call(wsb=16) == -4
+    assert call(wsp=0x70010) == -5                        # workspace not 256-byte aligned
+    assert call(T=0, x=0) == 0                            # empty batch: no launch

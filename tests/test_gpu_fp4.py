@@ -75,11 +75,47 @@ def qwen4(cuda_device):
     return W, _dev_weights(W, cuda_device)
 
 
-@pytest.mark.parametrize("B,tokens", [(4, range(4)), (32, [0, 13, 31])])
-def test_fp4_qwen_layer(cuda_device, qwen4, B, tokens):
+@pytest.mark.parametrize("B,routing", [(4, None), (8, None), (32, None), (32, "zipf")])
+def test_fp4_qwen_layer_every_token(cuda_device, qwen4, B, routing):
+    """The grouped MXFP4 kernels (every distinct expert's rows once per
+    call, experts with more than four tokens in several groups)."""
     W, Wd = qwen4
-    x, ids, w = inputs.layer_batch(inputs.QWEN3, B)
-    _compare(cuda_device, W, Wd, x, ids, w, tokens, f"fp4 qwen B={B}")
+    kw = {} if routing is None else {"routing": routing}
+    x, ids, w = inputs.layer_batch(inputs.QWEN3, B, **kw)
+    _compare(cuda_device, W, Wd, x, ids, w, range(B), f"fp4 qwen B={B} {routing}")
+
+
+def test_fp4_deepseek_shared_expert(cuda_device):
+    """The grouped MXFP4 kernels with the always-on shared expert."""
+    W = inputs.layer_weights(inputs.DEEPSEEK_V3, cuda_device, fp4=True)
+    Wd = _dev_weights(W, cuda_device)
+    x, ids, w = inputs.layer_batch(inputs.DEEPSEEK_V3, 8)
+    _compare(cuda_device, W, Wd, x, ids, w, range(8), "fp4 deepseek B=8")
+    del W, Wd
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("E,k,d,I", [(4, 2, 512, 256), (3, 3, 1056, 64)])
+def test_fp4_wide_scale_exponents(cuda_device, E, k, d, I):
+    """Scale bytes spread over 127 +- 20 (weights from 2^-20 to 2^20 times
+    their codes), on the grouped kernels (first shape) and the one-warp
+    kernels (second): each block's scale must multiply exactly its own
+    partial sum."""
+    cfg = inputs.LayerConfig(f"fp4_wide_{E}_{k}_{d}_{I}", E, k, d, I, True, "softmax_normal")
+    W = inputs.layer_weights(cfg, "cpu", fp4=True)
+    g = torch.Generator().manual_seed(11)
+    def spread(sc):
+        delta = torch.randint(-20, 21, sc.shape, generator=g, dtype=torch.int32)
+        return (sc.to(torch.int32) + delta).clamp(1, 254).to(torch.uint8)
+    for n in ("s_gate", "s_up", "s_down"):
+        W[n] = spread(W[n])
+    sh = list(W["shared"])
+    for i in (1, 3, 5):
+        sh[i] = spread(sh[i])
+    W["shared"] = tuple(sh)
+    Wd = _dev_weights(W, cuda_device)
+    x, ids, w = inputs.layer_batch(cfg, 5)
+    _compare(cuda_device, W, Wd, x, ids, w, range(5), f"fp4 wide scales {E},{k},{d},{I}")
 
 
 @pytest.mark.parametrize("E,k,d,I", [(5, 2, 96, 160), (3, 3, 1056, 64)])
