@@ -62,6 +62,12 @@ struct __align__(1024) GRStage {
     uint8_t raw[NB][GR_BN * GR_KC];   // [row][64] E4M3 codes as copied
 };
 
+// 16 bytes global -> shared (L2 only); src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async_16_plain(void* smem, const void* gmem, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(smem)), "l"(gmem), "r"(src_bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t swz128(int row, int chunk16) {
     return (uint32_t)(row * 128 + ((chunk16 ^ (row & 7)) << 4));
 }
@@ -130,7 +136,6 @@ __global__ void __launch_bounds__(GR_THREADS, 1) grouped_mma_kernel(GRArgs a) {
     uint8_t* scales = reinterpret_cast<uint8_t*>(stage + 2);  // [NB][GR_BN][nsc]
     uint64_t* bars = reinterpret_cast<uint64_t*>(scales + ((NB * GR_BN * nsc + 15) & ~15));
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int e = a.expert_ids[blk];
@@ -141,7 +146,6 @@ __global__ void __launch_bounds__(GR_THREADS, 1) grouped_mma_kernel(GRArgs a) {
     if (tid == 0) {
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
-        *abort_flag = 0;
         mbar_init_fence();
     }
     if (warp == 0) {  // tensor memory: NB x 128 FP32 columns
@@ -178,13 +182,13 @@ __global__ void __launch_bounds__(GR_THREADS, 1) grouped_mma_kernel(GRArgs a) {
                 src = reinterpret_cast<const char*>(a.a_src + ((int64_t)blk * GR_BM + row) * a.I +
                                                     (int64_t)kc * GR_KC) + c * 16;
             }
-            cp_async_16(reinterpret_cast<char*>(S.a) + swz128(row, c), src, bytes, 0);
+            cp_async_16_plain(reinterpret_cast<char*>(S.a) + swz128(row, c), src, bytes);
         }
         for (int p = 0; p < NB; ++p) {
             const uint8_t* wp = (p ? a.w1 : a.w0) + ((int64_t)e * rows_w + n0) * K + (int64_t)kc * GR_KC;
             for (int q = tid; q < GR_BN * 4; q += GR_THREADS) {
                 const int row = q >> 2, c = q & 3;
-                cp_async_16(S.raw[p] + row * GR_KC + c * 16, wp + (int64_t)row * K + c * 16, 16, 0);
+                cp_async_16_plain(S.raw[p] + row * GR_KC + c * 16, wp + (int64_t)row * K + c * 16, 16);
             }
         }
         cp_async_commit();
@@ -197,7 +201,8 @@ __global__ void __launch_bounds__(GR_THREADS, 1) grouped_mma_kernel(GRArgs a) {
         const int st = kc & 1;
         if (kc + 1 < NK) {
             // the MMAs of chunk kc - 1 read the other stage: wait before refilling it
-            if (kc >= 1 && !mbar_wait(&bars[(kc + 1) & 1], ((kc - 1) >> 1) & 1)) {
+            const bool done = kc < 1 || mbar_wait(&bars[(kc + 1) & 1], ((kc - 1) >> 1) & 1);
+            if (__syncthreads_or(!done)) {  // a wait gave up: every thread leaves together
                 ok = false;
                 break;
             }
@@ -246,13 +251,13 @@ __global__ void __launch_bounds__(GR_THREADS, 1) grouped_mma_kernel(GRArgs a) {
             umma_commit(&bars[st]);
         }
     }
+    cp_async_wait<0>();  // no copy still in flight on any exit from the loop
     // all MMAs done (they complete in order: the last commit covers them)
-    if (ok && !mbar_wait(&bars[(NK - 1) & 1], ((NK - 1) >> 1) & 1)) ok = false;
-    if (!ok) *abort_flag = 1;
+    const bool done = ok && mbar_wait(&bars[(NK - 1) & 1], ((NK - 1) >> 1) & 1);
+    const bool failed = __syncthreads_or(!done);
     tc_fence_after();
-    __syncthreads();
 
-    if (!*abort_flag) {
+    if (!failed) {
         const int m = warp * 32 + lane;                      // this thread's accumulator row
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         const int64_t srow = (int64_t)blk * GR_BM + m;
@@ -293,7 +298,7 @@ __global__ void __launch_bounds__(GR_THREADS, 1) grouped_mma_kernel(GRArgs a) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(NB * 128) : "memory");
     }
-    if (tid == 0 && *abort_flag) atomicOr(a.err, MOE_DEVERR_TIMEOUT);
+    if (tid == 0 && failed) atomicOr(a.err, MOE_DEVERR_TIMEOUT);
 }
 
 // y[t][o] = bf16( sum_j w[t][j] * out[t*k + j][o] ), j in order; a slot
@@ -313,7 +318,7 @@ __global__ void grouped_combine_kernel(const float* __restrict__ out, const floa
 
 template <int NB>
 static size_t grouped_smem(int K) {
-    return 1024 + 2 * sizeof(GRStage<NB>) + ((NB * GR_BN * (K / 32) + 15) & ~15) + 2 * sizeof(uint64_t) + 16;
+    return 1024 + 2 * sizeof(GRStage<NB>) + ((NB * GR_BN * (K / 32) + 15) & ~15) + 2 * sizeof(uint64_t) + 8;
 }
 
 template <int NB>

@@ -47,8 +47,9 @@ def device_mx(W, dev):
     return out
 
 
-def oracle_tokens(W, x, ids, w, tokens):
-    """Oracle layer for a subset of tokens, passing only the experts they touch."""
+def oracle_tokens(W, x, ids, w, tokens, mx_act=False):
+    """Oracle layer for a subset of tokens, passing only the experts they touch
+    (mx_act: the variant with x and h rounded through MXFP8)."""
     tokens = list(tokens)
     sub_ids = ids[tokens].cpu().numpy()
     uniq = sorted(set(sub_ids.reshape(-1).tolist()))
@@ -59,8 +60,9 @@ def oracle_tokens(W, x, ids, w, tokens):
     shared = None
     if W.get("shared") is not None:
         shared = tuple(t.cpu().numpy() for t in W["shared"])
-    return oracle.moe_layer(bf16_bits(x[tokens]), remap[sub_ids].astype(np.int32),
-                            w[tokens].cpu().numpy(), *host, shared=shared)
+    fn = oracle.moe_layer_mx_act if mx_act else oracle.moe_layer
+    return fn(bf16_bits(x[tokens]), remap[sub_ids].astype(np.int32), w[tokens].cpu().numpy(), *host,
+              shared=shared)
 
 
 def check_close(got: torch.Tensor, ref64: np.ndarray, what: str, allow=None):
