@@ -55,6 +55,9 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--ref-seconds", type=float, default=90.0)
+    p.add_argument("--profile", choices=["layer", "fp4", "grouped"], default=None,
+                   help="profiler run: --warmup + --steps plain calls of one path on the workload (one weight "
+                        "copy, no timing, no other sections), then exit")
     return p.parse_args(argv)
 
 
@@ -544,9 +547,73 @@ def run_fp4(dev, stream, ranks, cfg, B, routing, copy_gbs, K=100, n_batches=16):
         del W, bt
         torch.cuda.empty_cache()
         return {"workload": f"{cfg.name} B={B} routing={routing}, MXFP4 weights (E2M1, E8M0 per 32)",
-                "kernels": "gate_up_fp4_kernel + down_fp4_kernel (one warp per output value)",
+                "kernels": "the row-tile gate/up and down kernels with MXFP4 tiles (one warp per output "
+                           "value at B=1)",
                 "us": us, "gbs": gbs, "algorithmic_bytes_mean": mean_bytes,
                 "frac_of_copy_peak": gbs / copy_gbs}
+    except Exception as exc:  # reported, never fatal to the bench line
+        return {"error": repr(exc)[:300]}
+
+
+def run_grouped(dev, stream, ranks, hbm_peak, tensor_peak, reps, batches=(32, 64, 128, 256, 1024, 4096)):
+    """The expert-centric layer (moe_layer_grouped) against the decode layer
+    on the Qwen3-style workload, per B: µs of each (the decode layer up to its
+    B <= 256 limit), the grouped layer with MXFP8 activations too, and the
+    grouped layer's achieved HBM GB/s (algorithmic bytes: each distinct
+    expert's weights once, x, ids, w and y) and tensor TFLOP/s (2 * B * k * 3
+    * d * I).  One weight copy per replica, cycled; a failure leaves an
+    "error" field."""
+    try:
+        import torch
+        import mixture_experts_decode_gb300 as moe
+        from mixture_experts_decode_gb300 import inputs
+        cfg = inputs.QWEN3
+        rows = []
+        for B in batches:
+            n_b = 4
+            bt = [inputs.layer_batch(cfg, B, step=i) for i in range(n_b)]
+            by = [layer_bytes(cfg, ids, B) for _, ids, _ in bt]
+            dv = [(x.to(dev), i.to(dev), w.to(dev)) for x, i, w in bt]
+            ws = torch.empty(moe.layer_grouped_workspace_bytes(B, cfg.k, cfg.E, cfg.d, cfg.I),
+                             dtype=torch.uint8, device=dev)
+            y = torch.empty((B, cfg.d), dtype=torch.bfloat16, device=dev)
+
+            def grouped(i, act=False):
+                g, u, d, _ = reps[i % len(reps)]
+                x, ids, w = dv[i % n_b]
+                moe.layer_grouped(x, ids, w, g, u, d, act_mx=act, workspace=ws, y=y)
+
+            K = 40 if B <= 1024 else 10
+            gs, _, _ = time_steps(grouped, K, 3, stream, ranks, chunk=K, min_seconds=0.05, min_repeats=3,
+                                  max_repeats=10)
+            gms, _, _ = time_steps(lambda i: grouped(i, True), K, 3, stream, ranks, chunk=K, min_seconds=0.05,
+                                   min_repeats=3, max_repeats=10)
+            alg = statistics.mean(b["U"] for b in by) * 3 * cfg.I * cfg.d * 33 // 32 + 4 * B * cfg.d + 8 * B * cfg.k
+            flops = 2.0 * B * cfg.k * 3 * cfg.d * cfg.I
+            row = {"B": B, "grouped_us": gs / K * 1e6, "grouped_act_mx_us": gms / K * 1e6,
+                   "unique_experts_mean": statistics.mean(b["U"] for b in by),
+                   "grouped_gbs": alg / (gs / K) / 1e9, "grouped_frac_of_hbm_peak": alg / (gs / K) / 1e9 / hbm_peak,
+                   "grouped_tflops": flops / (gs / K) / 1e12,
+                   "grouped_frac_of_tensor_peak": flops / (gs / K) / 1e12 / tensor_peak}
+            if B <= 256:
+                wsd = torch.empty(moe.layer_workspace_bytes(B, cfg.k, cfg.I, False), dtype=torch.uint8, device=dev)
+
+                def decode(i):
+                    g, u, d, _ = reps[i % len(reps)]
+                    x, ids, w = dv[i % n_b]
+                    moe.layer(x, ids, w, g, u, d, workspace=wsd, y=y)
+
+                ds, _, _ = time_steps(decode, K, 3, stream, ranks, chunk=K, min_seconds=0.05, min_repeats=3,
+                                      max_repeats=10)
+                row["decode_us"] = ds / K * 1e6
+                row["faster"] = "grouped" if gs < ds else "decode"
+            rows.append(row)
+            del ws, dv
+        torch.cuda.empty_cache()
+        return {"workload": f"{cfg.name} routing={cfg.routing}, moe_layer_grouped vs moe_layer",
+                "kernels": "align + grouped_mma_kernel<2> (gate/up) + grouped_mma_kernel<1> (down) + combine; "
+                           "tcgen05.mma kind::f16, BF16 operands dequantised from MXFP8 in shared memory",
+                "tensor_peak_tflops": tensor_peak, "rows": rows}
     except Exception as exc:  # reported, never fatal to the bench line
         return {"error": repr(exc)[:300]}
 
@@ -663,6 +730,9 @@ def run_ours(args):
     wl_bytes = wl.bytes
     del wl
     torch.cuda.empty_cache()
+    tensor_peak = peaks.get("bf16_tflops") or 1900.0
+    grouped = None if args.no_sweep else run_grouped(dev, stream, ranks, hbm_peak, tensor_peak,
+                                                     qwen_reps[:2] or make_replicas(inputs.QWEN3, dev, 2))
     sw = None if args.no_sweep else sweep(dev, stream, ranks, hbm_peak, copy_gbs, qwen_reps)
 
     line = {
@@ -684,7 +754,7 @@ def run_ours(args):
         "kernels": {"gate_up_us": gu_us, "gate_up_gbs": gu_gbs, "down_us": dn_us, "down_gbs": dn_gbs},
         "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K * len(region_times), "clocks": clocks,
         "align": align, "align_zipf": align_zipf, "router": router, "mx_requant": requant, "fp4_layer": fp4,
-        "cpu_baseline": cpu, "sweep": sw,
+        "cpu_baseline": cpu, "grouped": grouped, "sweep": sw,
     }
     if ranks.rank == 0:
         print(json.dumps(line), flush=True)
@@ -751,9 +821,49 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """A short run of one path for a profiler (ncu) to capture: the decode
+    layer (gate/up + down), the same with MXFP4 weights (the two passes), or
+    the grouped layer; W + K calls on batches of the chosen workload."""
+    import torch
+    import __graft_entry__
+    import mixture_experts_decode_gb300 as moe
+    from mixture_experts_decode_gb300 import inputs
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    cfg = {"qwen3": inputs.QWEN3, "deepseek": inputs.DEEPSEEK_V3, "tiny": inputs.TINY}[args.config]
+    B = args.batch
+    W = inputs.layer_weights(cfg, dev, fp4=args.profile == "fp4")
+    mx = lambda a, b: moe.MX(W[a], W[b])
+    G, U, D = mx("w_gate", "s_gate"), mx("w_up", "s_up"), mx("w_down", "s_down")
+    sh = None
+    if W.get("shared") is not None:
+        s = W["shared"]
+        sh = (moe.MX(s[0], s[1]), moe.MX(s[2], s[3]), moe.MX(s[4], s[5]))
+    S = 1 if sh else 0
+    batches = [tuple(t.to(dev) for t in inputs.layer_batch(cfg, B, routing=args.routing, step=i)) for i in range(4)]
+    y = torch.empty((B, cfg.d), dtype=torch.bfloat16, device=dev)
+    h = torch.empty((B, cfg.k + S, cfg.I), dtype=torch.bfloat16, device=dev)
+    for i in range(args.warmup + args.steps):
+        x, ids, w = batches[i % len(batches)]
+        if args.profile == "layer":
+            moe.layer(x, ids, w, G, U, D, shared=sh, y=y)
+        elif args.profile == "fp4":
+            moe.gate_up(x, ids, G, U, shared_gate=sh[0] if sh else None, shared_up=sh[1] if sh else None,
+                        h=h, fp4=True)
+            moe.down(h, ids, w, D, shared_down=sh[2] if sh else None, y=y, fp4=True)
+        else:
+            moe.layer_grouped(x, ids, w, G, U, D, y=y)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": args.profile, "workload": f"{cfg.name} B={B} routing={args.routing}",
+                      "calls": args.warmup + args.steps, "device_error": moe.device_error(dev)}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -8,64 +8,77 @@
 // such grouped GEMMs).
 //
 //   gemm1 (gate/up): one CTA per (block of GR_BM sorted slots, GR_BN rows of
-//     I).  A = the slots' token rows of x (BF16; the pad slots zero), B = the
+//     I).  A = the block's real slots' token rows of x (BF16), B = the
 //     block's expert's W_gate and W_up rows, dequantised from MXFP8 to BF16
-//     in shared memory by the CTA's threads (exact: an E4M3 value times a
-//     power of two has at most four significant bits), D = two FP32
-//     accumulators in tensor memory.  Epilogue: h = bf16(SiLU(g) * u) per
-//     sorted slot.
-//   gemm2 (down): A = h of the block's slots, B = the expert's W_down rows,
-//     D = FP32 in tensor memory; the epilogue stores each real slot's row
-//     of partial outputs (FP32) at its flat slot index.
+//     in shared memory (exact for scale bytes >= 3: an E4M3 value times a
+//     power of two has at most four significant bits and stays a BF16
+//     normal), D = two FP32 accumulators in tensor memory.  Epilogue:
+//     h = bf16(SiLU(g) * u) per real slot, into h_sorted.
+//   gemm2 (down): A = the real slots' rows of h_sorted, B = the expert's
+//     W_down rows, D = FP32 in tensor memory; the epilogue stores each real
+//     slot's row of partial outputs (FP32) at its flat slot index.
 //   combine: y[t][o] = bf16( sum_j w[t][j] * out[t*k + j][o] ), the k slots
 //     in order.
 // Each MMA is tcgen05.mma kind::f16 (BF16 x BF16 -> FP32), M = 128, N =
 // 128, K = 16, issued by one thread from K-major 128-byte-swizzled shared
-// memory tiles; completion is signalled to an mbarrier by tcgen05.commit.
-// K advances in chunks of 64 through a two-stage ring: the copies of chunk
-// c + 1 (cp.async into the swizzled positions) and its dequantisation
-// overlap the MMAs of chunk c.  The products are those of the MX values
-// exactly; sums are FP32 (the tensor core's order).  With act_mx set, x and
-// h are first rounded through MXFP8 (moe_mx_requant): the conventional
+// memory tiles; tcgen05.commit signals completion to an mbarrier.  The pad
+// rows of a block's A tile are never written: they only feed accumulator
+// rows that no epilogue stores.  The products are those of the MX values
+// exactly; sums are FP32 in the tensor core's order.  With act_mx set, x
+// and h are first rounded through MXFP8 (moe_mx_requant): the conventional
 // path's activations.
 #include <cstdint>
 #include <mutex>
 
 #include "common.cuh"
+#include "decode_common.cuh"
 #include "internal.h"
 
 namespace moedec {
 
-constexpr int GR_BM = GROUPED_BLOCK;  // sorted slots per block (the MMA's M)
-constexpr int GR_BN = 128;   // weight rows per CTA (the MMA's N)
-constexpr int GR_KC = 64;    // K elements per chunk (one 128-byte swizzle row of BF16)
-constexpr int GR_THREADS = 128;
+constexpr int GR_BM = GROUPED_BLOCK;       // sorted slots per block (the MMA's M)
+constexpr int GR_BN = 128;                 // weight rows per CTA (the MMA's N)
+constexpr int GR_KC = 64;                  // K elements per chunk (one 128-byte swizzle row of BF16)
+constexpr int GR_CW = 8;                   // dequantising (consumer) warps
+constexpr int GR_THREADS = (GR_CW + 2) * 32;  // + the copy warp + the MMA warp
+constexpr int GR_MAXR = 8;                 // deepest ring of raw code stages
 
 struct GRArgs {
-    const uint16_t* a_src;     // gemm1: x [T][d] (rows by token); gemm2: h_sorted [n_sorted][I]
+    const uint16_t* a_src;     // gate/up: x [T][d] (rows by token); down: h_sorted [n_sorted][I]
     const int32_t* sorted;     // flat slot of each sorted row (T*k = pad)
     const int32_t* expert_ids; // expert of each block
     const int32_t* ntpp;       // rows used (a multiple of GR_BM)
-    const uint8_t *w0, *s0;    // gemm1: W_gate; gemm2: W_down (codes, E8M0 scales)
-    const uint8_t *w1, *s1;    // gemm1: W_up
-    uint16_t* h_sorted;        // gemm1 output [n_sorted][I] BF16
-    float* out;                // gemm2 output [T*k][d] FP32 by flat slot
+    const uint8_t *s0, *s1;    // E8M0 scales: gate/up: W_gate, W_up; down: W_down
+    uint16_t* h_sorted;        // gate/up output [n_sorted][I] BF16 (real rows only)
+    float* out;                // down output [T*k][d] FP32 by flat slot
     int T, k, E, d, I;
+    int NR;                    // raw code stages in the ring
     int* err;
 };
 
-// One stage: the A tile and each B matrix's raw codes and BF16 tile.
-template <int NB>
-struct __align__(1024) GRStage {
-    uint16_t a[GR_BM * GR_KC];        // [row][64] BF16, 128-byte swizzle (8-row atoms of 1024 B)
-    uint16_t b[NB][GR_BN * GR_KC];    // [row][64] BF16, same layout
-    uint8_t raw[NB][GR_BN * GR_KC];   // [row][64] E4M3 codes as copied
+// The weight codes' tensor maps: [E * rows][K] bytes, boxes of 64 x 128.
+struct GRMaps {
+    CUtensorMap w0, w1;
 };
 
-// 16 bytes global -> shared (L2 only); src_bytes = 0 writes zeros.
-__device__ __forceinline__ void cp_async_16_plain(void* smem, const void* gmem, int src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(smem)), "l"(gmem), "r"(src_bytes)
-                 : "memory");
+// Shared memory, byte offsets from a 1024-aligned base.
+struct GRLayout {
+    uint32_t a, bf, raw, scales, tok, bars, tmem_slot, abort, total;
+};
+
+__host__ __device__ inline GRLayout gr_layout(int NB, int K, int NR) {
+    GRLayout L;
+    uint32_t off = 0;
+    L.a = off;       off += 2 * 16384;                              // A tile per BF16 stage
+    L.bf = off;      off += 2 * NB * 16384;                         // dequantised B tiles
+    L.raw = off;     off += NR * NB * 8192;                         // raw E4M3 codes (TMA)
+    L.scales = off;  off += (NB * GR_BN * (K / 32) + 15) & ~15u;    // this CTA's weight rows' scales
+    L.tok = off;     off += GR_BM * 4;                              // source row of each real slot
+    L.bars = off;    off += (2 * GR_MAXR + 5) * 8;
+    L.tmem_slot = off; off += 8;
+    L.abort = off;   off += 8;
+    L.total = off;
+    return L;
 }
 
 __device__ __forceinline__ uint32_t swz128(int row, int chunk16) {
@@ -106,6 +119,11 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// 16 bytes global -> shared (L2 only).
+__device__ __forceinline__ void cp_async_16_plain(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem)), "l"(gmem) : "memory");
+}
+
 // 32 consecutive FP32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];
@@ -122,30 +140,62 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// NB = 2: gemm1 (gate, up; K = d, N over I); NB = 1: gemm2 (down; K = I, N over d).
+// One CTA = one block of GR_BM sorted slots (one expert) x GR_BN weight rows.
+// NB = 2: the gate/up GEMMs (K = d, N over I); NB = 1: the down GEMM (K = I,
+// N over d).  Warps 0..7 copy the A rows and dequantise the weight codes
+// into the BF16 tiles (and run the epilogue), warp 8 brings the raw codes by
+// TMA through an NR-stage ring, warp 9 issues the MMAs.  Barriers: raw_full
+// / raw_empty (the ring), bf_full (the 8 warps filled stage b) / bf_empty
+// (tcgen05.commit: the MMAs that read stage b finished), acc (all MMAs
+// done).  Every wait is bounded; a wait that gives up raises `abort`, after
+// which every role skips to the end (no copy left in flight, TMEM freed).
 template <int NB>
-__global__ void __launch_bounds__(GR_THREADS, 1) grouped_mma_kernel(GRArgs a) {
+__global__ void __launch_bounds__(GR_THREADS, NB == 1 ? 2 : 1) grouped_mma_kernel(GRArgs a, const __grid_constant__ GRMaps maps) {
     const int blk = blockIdx.x;
     if (blk * GR_BM >= *a.ntpp) return;  // a block past the used rows: nothing to do (uniform exit)
-    extern __shared__ __align__(128) unsigned char gr_smem[];
-    const uintptr_t base = (reinterpret_cast<uintptr_t>(gr_smem) + 1023) & ~uintptr_t(1023);
-    GRStage<NB>* stage = reinterpret_cast<GRStage<NB>*>(base);
-    const int K = NB == 2 ? a.d : a.I;         // contraction length
+    extern __shared__ __align__(1024) unsigned char gr_smem[];
+    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(gr_smem) + 1023) &
+                                                           ~uintptr_t(1023));
+    const int K = NB == 2 ? a.d : a.I;  // contraction length
     const int NK = K / GR_KC;
-    const int nsc = K / 32;                    // scale bytes per weight row
-    uint8_t* scales = reinterpret_cast<uint8_t*>(stage + 2);  // [NB][GR_BN][nsc]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(scales + ((NB * GR_BN * nsc + 15) & ~15));
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
+    const int nsc = K / 32;             // scale bytes per weight row
+    const int NR = a.NR;
+    const GRLayout L = gr_layout(NB, K, NR);
+    uint8_t* scales = base + L.scales;
+    int* tok = reinterpret_cast<int*>(base + L.tok);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bars);
+    uint64_t* raw_full = bars;
+    uint64_t* raw_empty = bars + GR_MAXR;
+    uint64_t* bf_full = bars + 2 * GR_MAXR;
+    uint64_t* bf_empty = bars + 2 * GR_MAXR + 2;
+    uint64_t* acc_full = bars + 2 * GR_MAXR + 4;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.tmem_slot);
+    volatile int* abort = reinterpret_cast<volatile int*>(base + L.abort);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int e = a.expert_ids[blk];
     const int n0 = blockIdx.y * GR_BN;
-    const int rows_w = NB == 2 ? a.I : a.d;    // weight rows per expert
+    const int rows_w = NB == 2 ? a.I : a.d;  // weight rows per expert
     const int64_t pad = (int64_t)a.T * a.k;
 
+    // the block's real slots (a prefix: the sort pads each expert's run at its end)
+    int real = 0;
+    if (tid < GR_BM) {
+        const int64_t f = a.sorted[(int64_t)blk * GR_BM + tid];
+        real = f < pad;
+        tok[tid] = real ? (NB == 2 ? (int)(f / a.k) : blk * GR_BM + tid) : 0;
+    }
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        for (int i = 0; i < NR; ++i) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_empty[i], GR_CW);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bf_full[i], GR_CW);
+            mbar_init(&bf_empty[i], 1);
+        }
+        mbar_init(acc_full, 1);
+        *abort = 0;
         mbar_init_fence();
     }
     if (warp == 0) {  // tensor memory: NB x 128 FP32 columns
@@ -156,138 +206,146 @@ __global__ void __launch_bounds__(GR_THREADS, 1) grouped_mma_kernel(GRArgs a) {
     }
     // this CTA's weight rows' scale bytes (32-bit loads: K % 128 == 0 keeps rows 4-byte aligned)
     for (int p = 0; p < NB; ++p) {
-        const uint8_t* sp = (p ? a.s1 : a.s0) + ((int64_t)e * rows_w + n0) * nsc;
-        const int words = GR_BN * nsc / 4;
-        for (int i = tid; i < words; i += GR_THREADS)
-            reinterpret_cast<uint32_t*>(scales + p * GR_BN * nsc)[i] = reinterpret_cast<const uint32_t*>(sp)[i];
+        const uint32_t* sp =
+            reinterpret_cast<const uint32_t*>((p ? a.s1 : a.s0) + ((int64_t)e * rows_w + n0) * nsc);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(scales + p * GR_BN * nsc);
+        for (int i = tid; i < GR_BN * nsc / 4; i += GR_THREADS) dst[i] = sp[i];
     }
     tc_fence_before();
-    __syncthreads();
+    const int nreal = __syncthreads_count(real);
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // source row of each of this thread's A rows (8 chunks of 16 B per row, 8 threads per row)
-    auto issue_chunk = [&](int kc, int st) {
-        GRStage<NB>& S = stage[st];
-        for (int q = tid; q < GR_BM * 8; q += GR_THREADS) {
-            const int row = q >> 3, c = q & 7;
-            const char* src;
-            int bytes = 16;
-            if (NB == 2) {
-                const int64_t f = a.sorted[(int64_t)blk * GR_BM + row];
-                const int64_t t = f < pad ? f / a.k : 0;
-                if (f >= pad) bytes = 0;  // pad slot: zero row
-                src = reinterpret_cast<const char*>(a.a_src + t * a.d + (int64_t)kc * GR_KC) + c * 16;
-            } else {
-                src = reinterpret_cast<const char*>(a.a_src + ((int64_t)blk * GR_BM + row) * a.I +
-                                                    (int64_t)kc * GR_KC) + c * 16;
-            }
-            cp_async_16_plain(reinterpret_cast<char*>(S.a) + swz128(row, c), src, bytes);
-        }
-        for (int p = 0; p < NB; ++p) {
-            const uint8_t* wp = (p ? a.w1 : a.w0) + ((int64_t)e * rows_w + n0) * K + (int64_t)kc * GR_KC;
-            for (int q = tid; q < GR_BN * 4; q += GR_THREADS) {
-                const int row = q >> 2, c = q & 3;
-                cp_async_16_plain(S.raw[p] + row * GR_KC + c * 16, wp + (int64_t)row * K + c * 16, 16);
-            }
-        }
-        cp_async_commit();
-    };
-
-    constexpr uint32_t IDESC = gr_idesc(GR_BM, GR_BN);
-    issue_chunk(0, 0);
-    bool ok = true;
-    for (int kc = 0; kc < NK; ++kc) {
-        const int st = kc & 1;
-        if (kc + 1 < NK) {
-            // the MMAs of chunk kc - 1 read the other stage: wait before refilling it
-            const bool done = kc < 1 || mbar_wait(&bars[(kc + 1) & 1], ((kc - 1) >> 1) & 1);
-            if (__syncthreads_or(!done)) {  // a wait gave up: every thread leaves together
-                ok = false;
-                break;
-            }
-            issue_chunk(kc + 1, (kc + 1) & 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-        // dequantise this chunk's weight rows: item = (row, 16 codes)
-        GRStage<NB>& S = stage[st];
-        for (int p = 0; p < NB; ++p) {
-            for (int q = tid; q < GR_BN * 4; q += GR_THREADS) {
-                const int row = q >> 2, c = q & 3;
-                const uint4 w4 = *reinterpret_cast<const uint4*>(S.raw[p] + row * GR_KC + c * 16);
-                const float sc = e8m0_to_float(scales[p * GR_BN * nsc + row * nsc + kc * 2 + (c >> 1)]);
-                uint32_t o[8];
+    if (warp == GR_CW) {
+        // ---------------- copy warp: raw codes by TMA ----------------
+        if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();
+            const int wrow = e * rows_w + n0;
+            int issued = 0;
+            for (int kc = 0; kc < NK; ++kc) {
+                const int r = kc % NR;
+                if (kc >= NR && !mbar_wait_abort(&raw_empty[r], ((kc / NR) - 1) & 1, abort)) break;
+                mbar_arrive_expect_tx(&raw_full[r], NB * 8192);
 #pragma unroll
-                for (int wq = 0; wq < 4; ++wq) {
-                    float2 lo, hi;
-                    e4m3x4_to_float((&w4.x)[wq], lo, hi);
-                    const __nv_bfloat162 b0 = __floats2bfloat162_rn(lo.x * sc, lo.y * sc);
-                    const __nv_bfloat162 b1 = __floats2bfloat162_rn(hi.x * sc, hi.y * sc);
-                    memcpy(&o[wq * 2], &b0, 4);
-                    memcpy(&o[wq * 2 + 1], &b1, 4);
-                }
-                char* dst = reinterpret_cast<char*>(S.b[p]);
-                *reinterpret_cast<uint4*>(dst + swz128(row, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
-                *reinterpret_cast<uint4*>(dst + swz128(row, 2 * c + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+                for (int p = 0; p < NB; ++p)
+                    tma_2d(base + L.raw + (r * NB + p) * 8192, p ? &maps.w1 : &maps.w0, kc * GR_KC, wrow,
+                           &raw_full[r], pol);
+                ++issued;
             }
+            // never leave the CTA with a copy in flight
+            for (int j = issued > NR ? issued - NR : 0; j < issued; ++j) mbar_wait(&raw_full[j % NR], (j / NR) & 1);
         }
-        fence_proxy_async();  // the tiles' generic-proxy writes, before the tensor cores read them
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t a0 = smem_addr(S.a);
+    } else if (warp == GR_CW + 1) {
+        // ---------------- MMA warp ----------------
+        if (lane == 0) {
+            constexpr uint32_t IDESC = gr_idesc(GR_BM, GR_BN);
+            int kc = 0;
+            for (; kc < NK; ++kc) {
+                const int b = kc & 1;
+                if (!mbar_wait_abort(&bf_full[b], (kc >> 1) & 1, abort)) break;
+                fence_proxy_async();
+                tc_fence_after();
+                const uint32_t a0 = smem_addr(base + L.a + b * 16384);
+#pragma unroll
+                for (int p = 0; p < NB; ++p) {
+                    const uint32_t b0 = smem_addr(base + L.bf + (b * NB + p) * 16384);
+#pragma unroll
+                    for (int kk = 0; kk < GR_KC / 16; ++kk)
+                        umma_bf16(tmem + p * 128, umma_desc_sw128(a0 + kk * 32), umma_desc_sw128(b0 + kk * 32),
+                                  IDESC, (kc > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(&bf_empty[b]);
+            }
+            if (kc == NK)
+                umma_commit(acc_full);
+            else if (kc > 0)  // gave up: let the MMAs already issued finish before TMEM is freed
+                mbar_wait(&bf_empty[(kc - 1) & 1], ((kc - 1) >> 1) & 1);
+        }
+    } else {
+        // ---------------- consumers: A rows + dequantisation ----------------
+        const int ct = tid;  // 0 .. GR_CW*32-1
+        for (int kc = 0; kc < NK; ++kc) {
+            const int b = kc & 1, r = kc % NR;
+            // the MMAs that read stage b two chunks ago must be done
+            if (kc >= 2 && !__all_sync(FULL_MASK, mbar_wait_abort(&bf_empty[b], ((kc >> 1) - 1) & 1, abort))) break;
+            unsigned char* As = base + L.a + b * 16384;
+            const int64_t rs = NB == 2 ? a.d : a.I;  // A row stride in elements
+            for (int q = ct; q < nreal * 8; q += GR_CW * 32) {
+                const int row = q >> 3, c = q & 7;
+                cp_async_16_plain(As + swz128(row, c), a.a_src + (int64_t)tok[row] * rs + kc * GR_KC + c * 8);
+            }
+            cp_async_commit();
+            if (!__all_sync(FULL_MASK, mbar_wait_abort(&raw_full[r], (kc / NR) & 1, abort))) break;
 #pragma unroll
             for (int p = 0; p < NB; ++p) {
-                const uint32_t b0 = smem_addr(S.b[p]);
+                const uint8_t* raw = base + L.raw + (r * NB + p) * 8192;
+                char* dst = reinterpret_cast<char*>(base + L.bf + (b * NB + p) * 16384);
+                const uint8_t* sc_row = scales + p * GR_BN * nsc + kc * 2;
 #pragma unroll
-                for (int kk = 0; kk < GR_KC / 16; ++kk)
-                    umma_bf16(tmem + p * 128, umma_desc_sw128(a0 + kk * 32), umma_desc_sw128(b0 + kk * 32), IDESC,
-                              (kc > 0 || kk > 0) ? 1u : 0u);
-            }
-            umma_commit(&bars[st]);
-        }
-    }
-    cp_async_wait<0>();  // no copy still in flight on any exit from the loop
-    // all MMAs done (they complete in order: the last commit covers them)
-    const bool done = ok && mbar_wait(&bars[(NK - 1) & 1], ((NK - 1) >> 1) & 1);
-    const bool failed = __syncthreads_or(!done);
-    tc_fence_after();
-
-    if (!failed) {
-        const int m = warp * 32 + lane;                      // this thread's accumulator row
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-        const int64_t srow = (int64_t)blk * GR_BM + m;
-        const int64_t f = a.sorted[srow];
-        if (NB == 2) {
-            for (int c0 = 0; c0 < GR_BN; c0 += 32) {
-                float g[32], u[32];
-                tmem_ld32(lane_base + c0, g);
-                tmem_ld32(lane_base + 128 + c0, u);
-                uint32_t o[16];
+                for (int i = 0; i < GR_BN * 4 / (GR_CW * 32); ++i) {
+                    const int q = ct + i * GR_CW * 32;
+                    const int row = q >> 2, c = q & 3;
+                    const uint4 w4 = *reinterpret_cast<const uint4*>(raw + row * GR_KC + c * 16);
+                    const float sc = e8m0_to_float(sc_row[row * nsc + (c >> 1)]);
+                    uint32_t o[8];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float h0 = g[2 * i] / (1.0f + expf(-g[2 * i])) * u[2 * i];
-                    float h1 = g[2 * i + 1] / (1.0f + expf(-g[2 * i + 1])) * u[2 * i + 1];
-                    if (f >= pad) h0 = h1 = 0.f;
-                    const __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
-                    memcpy(&o[i], &hb, 4);
+                    for (int wq = 0; wq < 4; ++wq) {
+                        float2 lo, hi;
+                        e4m3x4_to_float((&w4.x)[wq], lo, hi);
+                        const __nv_bfloat162 b0 = __floats2bfloat162_rn(lo.x * sc, lo.y * sc);
+                        const __nv_bfloat162 b1 = __floats2bfloat162_rn(hi.x * sc, hi.y * sc);
+                        memcpy(&o[wq * 2], &b0, 4);
+                        memcpy(&o[wq * 2 + 1], &b1, 4);
+                    }
+                    *reinterpret_cast<uint4*>(dst + swz128(row, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4*>(dst + swz128(row, 2 * c + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
                 }
-                uint4* dst = reinterpret_cast<uint4*>(a.h_sorted + srow * a.I + n0 + c0);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
             }
-        } else {
-            for (int c0 = 0; c0 < GR_BN; c0 += 32) {
-                float v[32];
-                tmem_ld32(lane_base + c0, v);
-                if (f < pad) {
-                    float4* dst = reinterpret_cast<float4*>(a.out + f * a.d + n0 + c0);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&raw_empty[r]);
+            cp_async_wait<0>();
+            fence_proxy_async();  // this thread's tile writes, before the tensor cores read them
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bf_full[b]);
+        }
+        cp_async_wait<0>();  // no copy still in flight on any exit from the loop
+        // ---------------- epilogue: TMEM -> h (gate/up) or the slots' partial outputs (down) ----------------
+        if (__all_sync(FULL_MASK, mbar_wait_abort(acc_full, 0, abort))) {
+            tc_fence_after();
+            const int m = (warp & 3) * 32 + lane;            // accumulator row = TMEM lane
+            const int cb = (warp >> 2) * 64;                 // this warp's 64 columns
+            const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+            const int64_t srow = (int64_t)blk * GR_BM + m;
+#pragma unroll 1
+            for (int c0 = cb; c0 < cb + 64; c0 += 32) {
+                if (NB == 2) {
+                    float g[32], u[32];
+                    tmem_ld32(lane_base + c0, g);
+                    tmem_ld32(lane_base + 128 + c0, u);
+                    if (m < nreal) {
+                        uint32_t o[16];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                        for (int i = 0; i < 16; ++i) {
+                            const float h0 = g[2 * i] / (1.0f + expf(-g[2 * i])) * u[2 * i];
+                            const float h1 = g[2 * i + 1] / (1.0f + expf(-g[2 * i + 1])) * u[2 * i + 1];
+                            const __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
+                            memcpy(&o[i], &hb, 4);
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(a.h_sorted + srow * a.I + n0 + c0);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    }
+                } else {
+                    float v[32];
+                    tmem_ld32(lane_base + c0, v);
+                    if (m < nreal) {
+                        const int64_t f = a.sorted[srow];
+                        float4* dst = reinterpret_cast<float4*>(a.out + f * a.d + n0 + c0);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    }
                 }
             }
         }
@@ -298,7 +356,7 @@ __global__ void __launch_bounds__(GR_THREADS, 1) grouped_mma_kernel(GRArgs a) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(NB * 128) : "memory");
     }
-    if (tid == 0 && failed) atomicOr(a.err, MOE_DEVERR_TIMEOUT);
+    if (tid == 0 && *abort) atomicOr(a.err, MOE_DEVERR_TIMEOUT);
 }
 
 // y[t][o] = bf16( sum_j w[t][j] * out[t*k + j][o] ), j in order; a slot
@@ -316,16 +374,23 @@ __global__ void grouped_combine_kernel(const float* __restrict__ out, const floa
     }
 }
 
-template <int NB>
-static size_t grouped_smem(int K) {
-    return 1024 + 2 * sizeof(GRStage<NB>) + ((NB * GR_BN * (K / 32) + 15) & ~15) + 2 * sizeof(uint64_t) + 8;
+// Raw-code ring depth: as deep as the shared memory allows, 2 .. GR_MAXR
+// (the down pass keeps two CTAs per SM).
+static int grouped_ring(int NB, int K, int max_smem) {
+    int NR = NB == 2 ? 6 : 4;
+    while (NR > 2 && gr_layout(NB, K, NR).total + 1024 > (uint32_t)max_smem) --NR;
+    return NR;
 }
 
 template <int NB>
-static cudaError_t launch_grouped_mma(const GRArgs& a, int64_t n_blocks, int ntile, size_t smem, int dev,
-                                      cudaStream_t st) {
+static cudaError_t launch_grouped_mma(GRArgs a, const GRMaps& maps, int64_t n_blocks, int ntile, int max_smem,
+                                      int dev, cudaStream_t st) {
     static std::mutex mu;
     static size_t attr[64] = {0};
+    const int K = NB == 2 ? a.d : a.I;
+    a.NR = grouped_ring(NB, K, max_smem);
+    const size_t smem = gr_layout(NB, K, a.NR).total + 1024;
+    if (smem > (size_t)max_smem) return cudaErrorInvalidValue;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -336,13 +401,15 @@ static cudaError_t launch_grouped_mma(const GRArgs& a, int64_t n_blocks, int nti
             attr[dev] = smem;
         }
     }
-    grouped_mma_kernel<NB><<<dim3((unsigned)n_blocks, (unsigned)ntile), GR_THREADS, smem, st>>>(a);
+    grouped_mma_kernel<NB><<<dim3((unsigned)n_blocks, (unsigned)ntile), GR_THREADS, smem, st>>>(a, maps);
     return cudaGetLastError();
 }
 
-bool grouped_shape_ok(int d, int I) { return d % GR_BN == 0 && I % GR_BN == 0 && d % 128 == 0 && I % 128 == 0; }
+bool grouped_shape_ok(int d, int I) { return d % 128 == 0 && I % 128 == 0; }
 
-size_t grouped_smem_bytes(int d, int I) { return std::max(grouped_smem<2>(d), grouped_smem<1>(I)); }
+size_t grouped_smem_bytes(int d, int I) {
+    return std::max(gr_layout(2, d, 2).total, gr_layout(1, I, 2).total) + 1024;
+}
 
 cudaError_t launch_grouped(const uint16_t* x, int T, int d, const int32_t* ids, const float* w, int k, MXView wg,
                            MXView wu, MXView wd, int E, int I, bool act_mx, const GroupedWorkspace& ws, uint16_t* y,
@@ -352,6 +419,12 @@ cudaError_t launch_grouped(const uint16_t* x, int T, int d, const int32_t* ids, 
     if (err != cudaSuccess) return err;
     int dev = 0;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    GRMaps m1{}, m2{};
+    if (!map_2d_u8(&m1.w0, wg.w, (uint64_t)E * I, d, GR_BN, GR_KC) ||
+        !map_2d_u8(&m1.w1, wu.w, (uint64_t)E * I, d, GR_BN, GR_KC) ||
+        !map_2d_u8(&m2.w0, wd.w, (uint64_t)E * d, I, GR_BN, GR_KC))
+        return cudaErrorInvalidValue;
+    m2.w1 = m2.w0;
     err = launch_align(ids, T, k, E, GR_BM, ws.sorted, ws.n_sorted, ws.expert_ids, ws.n_blocks, ws.ntpp, ws.align_ws,
                        st);
     if (err != cudaSuccess) return err;
@@ -373,19 +446,16 @@ cudaError_t launch_grouped(const uint16_t* x, int T, int d, const int32_t* ids, 
     a.I = I;
     a.err = di.err_word;
     a.a_src = xa;
-    a.w0 = wg.w;
     a.s0 = wg.s;
-    a.w1 = wu.w;
     a.s1 = wu.s;
-    if ((err = launch_grouped_mma<2>(a, ws.n_blocks, I / GR_BN, grouped_smem<2>(d), dev, st)) != cudaSuccess)
+    if ((err = launch_grouped_mma<2>(a, m1, ws.n_blocks, I / GR_BN, di.max_smem_optin, dev, st)) != cudaSuccess)
         return err;
+    // only the real rows of h_sorted were written: round those (and harmless pad-row bits) through MXFP8
     if (act_mx && (err = launch_mx_requant(ws.h_sorted, ws.h_sorted, ws.n_sorted, I, st)) != cudaSuccess) return err;
     a.a_src = ws.h_sorted;
-    a.w0 = wd.w;
     a.s0 = wd.s;
-    a.w1 = nullptr;
     a.s1 = nullptr;
-    if ((err = launch_grouped_mma<1>(a, ws.n_blocks, d / GR_BN, grouped_smem<1>(I), dev, st)) != cudaSuccess)
+    if ((err = launch_grouped_mma<1>(a, m2, ws.n_blocks, d / GR_BN, di.max_smem_optin, dev, st)) != cudaSuccess)
         return err;
     const int64_t n = (int64_t)T * d;
     const int64_t grid = std::min<int64_t>((n + 255) / 256, (int64_t)di.sm_count * 8);
