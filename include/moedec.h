@@ -210,13 +210,13 @@ int moe_layer_host(const void* x_host, int B, int d, const int32_t* topk_ids_hos
  *   x         BF16 [T][d], 32-byte aligned.  topk_ids int32 [T][k]; an id
  *             outside [0, E) adds nothing and sets MOE_DEVERR_EXPERT_ID.
  *   topk_w    float32 [T][k].  weights as for moe_layer; each scale array
- *             4-byte aligned.
+ *             16-byte aligned.
  *   d, I      multiples of 128.  E <= MOE_ALIGN_MAX_EXPERTS; T*k +
  *             E*127 < 2^31.  No limit on T beyond that.
  *   act_mx    0: activations as given (the decode layer's numerics);
  *             1: x and h rounded through MXFP8, the conventional path.
  *   workspace >= moe_layer_grouped_workspace_bytes(), 256-byte aligned.
- *   y         BF16 [T][d].
+ *   y         BF16 [T][d], 8-byte aligned.
  * Errors: MOE_ERR_SHAPE (d or I not a multiple of 128, k > E),
  * MOE_ERR_LIMIT, MOE_ERR_WORKSPACE, MOE_ERR_ALIGN, MOE_ERR_CUDA.
  */

@@ -344,8 +344,8 @@ int moe_layer_grouped(const void* x, int T, int d, const int32_t* topk_ids, cons
     if (T == 0) return MOE_OK;
     if (!x || !topk_ids || !topk_w || !y) return MOE_ERR_ARG;
     if ((rc = check_mx(w_gate)) || (rc = check_mx(w_up)) || (rc = check_mx(w_down))) return rc;
-    if (!aligned(w_gate.s, 4) || !aligned(w_up.s, 4) || !aligned(w_down.s, 4)) return MOE_ERR_ALIGN;
-    if (!aligned(x, 32) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(y, 2)) return MOE_ERR_ALIGN;
+    if (!aligned(w_gate.s, 16) || !aligned(w_up.s, 16) || !aligned(w_down.s, 16)) return MOE_ERR_ALIGN;
+    if (!aligned(x, 32) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(y, 8)) return MOE_ERR_ALIGN;
     const size_t need = grouped_carve(T, k, E, d, I, nullptr, nullptr);
     if (!workspace || workspace_bytes < need) return MOE_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return MOE_ERR_ALIGN;

@@ -37,10 +37,12 @@
 namespace moedec {
 
 constexpr int GR_BM = GROUPED_BLOCK;       // sorted slots per block (the MMA's M)
-constexpr int GR_BN = 128;                 // weight rows per CTA (the MMA's N)
+constexpr int GR_BN = 128;                 // weight rows per tile (the MMA's N)
 constexpr int GR_KC = 64;                  // K elements per chunk (one 128-byte swizzle row of BF16)
-constexpr int GR_CW = 8;                   // dequantising (consumer) warps
-constexpr int GR_THREADS = (GR_CW + 2) * 32;  // + the copy warp + the MMA warp
+constexpr int GR_CW = 8;                   // dequantising (consumer) warps: 0 .. 7
+constexpr int GR_PW = GR_CW;               // the copy warp
+constexpr int GR_MW = GR_CW + 1;           // the MMA warp
+constexpr int GR_THREADS = (GR_CW + 6) * 32;  // + four epilogue warps (10 .. 13: TMEM lane quadrants 2, 3, 0, 1)
 constexpr int GR_MAXR = 8;                 // deepest ring of raw code stages
 
 struct GRArgs {
@@ -53,6 +55,7 @@ struct GRArgs {
     float* out;                // down output [T*k][d] FP32 by flat slot
     int T, k, E, d, I;
     int NR;                    // raw code stages in the ring
+    int TB;                    // per-tile buffers (scales + sorted rows): 1 or 2
     int* err;
 };
 
@@ -63,20 +66,20 @@ struct GRMaps {
 
 // Shared memory, byte offsets from a 1024-aligned base.
 struct GRLayout {
-    uint32_t a, bf, raw, scales, tok, bars, tmem_slot, abort, total;
+    uint32_t a, bf, raw, tile, tile_bytes, bars, tmem_slot, abort, total;
 };
 
-__host__ __device__ inline GRLayout gr_layout(int NB, int K, int NR) {
+__host__ __device__ inline GRLayout gr_layout(int NB, int K, int NR, int TB) {
     GRLayout L;
     uint32_t off = 0;
-    L.a = off;       off += 2 * 16384;                              // A tile per BF16 stage
-    L.bf = off;      off += 2 * NB * 16384;                         // dequantised B tiles
-    L.raw = off;     off += NR * NB * 8192;                         // raw E4M3 codes (TMA)
-    L.scales = off;  off += (NB * GR_BN * (K / 32) + 15) & ~15u;    // this CTA's weight rows' scales
-    L.tok = off;     off += GR_BM * 4;                              // source row of each real slot
-    L.bars = off;    off += (2 * GR_MAXR + 5) * 8;
-    L.tmem_slot = off; off += 8;
-    L.abort = off;   off += 8;
+    L.a = off;          off += 2 * 16384;                              // A tile per BF16 stage
+    L.bf = off;         off += 2 * NB * 16384;                         // dequantised B tiles
+    L.raw = off;        off += NR * NB * 8192;                         // raw E4M3 codes (TMA ring)
+    L.tile_bytes = NB * GR_BN * (K / 32) + GR_BM * 4;                  // a tile's scales + sorted rows
+    L.tile = off;       off += TB * L.tile_bytes;
+    L.bars = off;       off += (2 * GR_MAXR + 12) * 8;
+    L.tmem_slot = off;  off += 8;
+    L.abort = off;      off += 8;
     L.total = off;
     return L;
 }
@@ -140,51 +143,54 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// One CTA = one block of GR_BM sorted slots (one expert) x GR_BN weight rows.
+// A persistent CTA works through tiles t = blockIdx.x, + gridDim.x, ...; a
+// tile is (block of GR_BM sorted slots of one expert, GR_BN weight rows).
 // NB = 2: the gate/up GEMMs (K = d, N over I); NB = 1: the down GEMM (K = I,
-// N over d).  Warps 0..7 copy the A rows and dequantise the weight codes
-// into the BF16 tiles (and run the epilogue), warp 8 brings the raw codes by
-// TMA through an NR-stage ring, warp 9 issues the MMAs.  Barriers: raw_full
-// / raw_empty (the ring), bf_full (the 8 warps filled stage b) / bf_empty
-// (tcgen05.commit: the MMAs that read stage b finished), acc (all MMAs
-// done).  Every wait is bounded; a wait that gives up raises `abort`, after
-// which every role skips to the end (no copy left in flight, TMEM freed).
+// N over d).  Roles, all overlapped across tiles:
+//   copy warp      per tile: the tile's scale rows and sorted slots (1D bulk
+//                  copies); per K chunk: the raw codes (2D TMA) into an
+//                  NR-stage ring;
+//   warps 0..7     per chunk: the real rows of A (cp.async into the 128-byte
+//                  swizzle) and the dequantisation of the codes into BF16
+//                  tiles (two stages);
+//   MMA warp       per chunk: NB x 4 tcgen05.mma into one of two TMEM
+//                  accumulators (alternating by tile);
+//   warps 10..13   per tile: the epilogue from TMEM (one lane quadrant each).
+// Barriers: raw_full/raw_empty (ring), bf_full/bf_empty (BF16 stages; empty
+// by tcgen05.commit), tile_full/tile_empty (per-tile buffers), acc_full
+// (commit) / acc_empty (epilogue done with an accumulator).  Every wait is
+// bounded; one that gives up raises `abort` and every role skips to the end
+// (copies drained, MMAs finished, TMEM freed).
 template <int NB>
 __global__ void __launch_bounds__(GR_THREADS, NB == 1 ? 2 : 1) grouped_mma_kernel(GRArgs a, const __grid_constant__ GRMaps maps) {
-    const int blk = blockIdx.x;
-    if (blk * GR_BM >= *a.ntpp) return;  // a block past the used rows: nothing to do (uniform exit)
+    const int ntile = (NB == 2 ? a.I : a.d) / GR_BN;
+    const int n_tiles = (*a.ntpp / GR_BM) * ntile;
+    if ((int)blockIdx.x >= n_tiles) return;  // uniform: no tile for this CTA
     extern __shared__ __align__(1024) unsigned char gr_smem[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(gr_smem) + 1023) &
                                                            ~uintptr_t(1023));
     const int K = NB == 2 ? a.d : a.I;  // contraction length
     const int NK = K / GR_KC;
     const int nsc = K / 32;             // scale bytes per weight row
-    const int NR = a.NR;
-    const GRLayout L = gr_layout(NB, K, NR);
-    uint8_t* scales = base + L.scales;
-    int* tok = reinterpret_cast<int*>(base + L.tok);
+    const int NR = a.NR, TB = a.TB;
+    const GRLayout L = gr_layout(NB, K, NR, TB);
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bars);
     uint64_t* raw_full = bars;
     uint64_t* raw_empty = bars + GR_MAXR;
     uint64_t* bf_full = bars + 2 * GR_MAXR;
-    uint64_t* bf_empty = bars + 2 * GR_MAXR + 2;
-    uint64_t* acc_full = bars + 2 * GR_MAXR + 4;
+    uint64_t* bf_empty = bf_full + 2;
+    uint64_t* tile_full = bf_full + 4;
+    uint64_t* tile_empty = bf_full + 6;
+    uint64_t* acc_full = bf_full + 8;
+    uint64_t* acc_empty = bf_full + 10;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.tmem_slot);
     volatile int* abort = reinterpret_cast<volatile int*>(base + L.abort);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int e = a.expert_ids[blk];
-    const int n0 = blockIdx.y * GR_BN;
     const int rows_w = NB == 2 ? a.I : a.d;  // weight rows per expert
-    const int64_t pad = (int64_t)a.T * a.k;
+    const int pad = a.T * a.k;
+    const int n_my = (n_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;  // tiles of this CTA
 
-    // the block's real slots (a prefix: the sort pads each expert's run at its end)
-    int real = 0;
-    if (tid < GR_BM) {
-        const int64_t f = a.sorted[(int64_t)blk * GR_BM + tid];
-        real = f < pad;
-        tok[tid] = real ? (NB == 2 ? (int)(f / a.k) : blk * GR_BM + tid) : 0;
-    }
     if (tid == 0) {
         for (int i = 0; i < NR; ++i) {
             mbar_init(&raw_full[i], 1);
@@ -193,141 +199,201 @@ __global__ void __launch_bounds__(GR_THREADS, NB == 1 ? 2 : 1) grouped_mma_kerne
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bf_full[i], GR_CW);
             mbar_init(&bf_empty[i], 1);
+            mbar_init(&tile_full[i], 1);
+            mbar_init(&tile_empty[i], GR_CW + 4);
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 4);
         }
-        mbar_init(acc_full, 1);
         *abort = 0;
         mbar_init_fence();
     }
-    if (warp == 0) {  // tensor memory: NB x 128 FP32 columns
+    if (warp == 0) {  // tensor memory: two accumulators of NB x 128 FP32 columns
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
-                     "r"(NB * 128)
+                     "r"(2 * NB * 128)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    // this CTA's weight rows' scale bytes (32-bit loads: K % 128 == 0 keeps rows 4-byte aligned)
-    for (int p = 0; p < NB; ++p) {
-        const uint32_t* sp =
-            reinterpret_cast<const uint32_t*>((p ? a.s1 : a.s0) + ((int64_t)e * rows_w + n0) * nsc);
-        uint32_t* dst = reinterpret_cast<uint32_t*>(scales + p * GR_BN * nsc);
-        for (int i = tid; i < GR_BN * nsc / 4; i += GR_THREADS) dst[i] = sp[i];
-    }
     tc_fence_before();
-    const int nreal = __syncthreads_count(real);
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == GR_CW) {
-        // ---------------- copy warp: raw codes by TMA ----------------
+    if (warp == GR_PW) {
+        // ---------------- copy warp ----------------
         if (lane == 0) {
             const uint64_t pol = l2_evict_first_policy();
-            const int wrow = e * rows_w + n0;
-            int issued = 0;
-            for (int kc = 0; kc < NK; ++kc) {
-                const int r = kc % NR;
-                if (kc >= NR && !mbar_wait_abort(&raw_empty[r], ((kc / NR) - 1) & 1, abort)) break;
-                mbar_arrive_expect_tx(&raw_full[r], NB * 8192);
-#pragma unroll
+            int g = 0, li = 0;  // chunks and tiles issued
+            bool ok = true;
+            for (; li < n_my && ok; ++li) {
+                const int t = (int)blockIdx.x + li * (int)gridDim.x;
+                const int blk = t / ntile, n0 = (t - blk * ntile) * GR_BN;
+                const int e = a.expert_ids[blk];
+                const int wrow = e * rows_w + n0;
+                const int tb = li % TB;
+                if (li >= TB && !mbar_wait_abort(&tile_empty[tb], ((li / TB) - 1) & 1, abort)) break;
+                unsigned char* tbuf = base + L.tile + tb * L.tile_bytes;
+                mbar_arrive_expect_tx(&tile_full[tb], L.tile_bytes);
                 for (int p = 0; p < NB; ++p)
-                    tma_2d(base + L.raw + (r * NB + p) * 8192, p ? &maps.w1 : &maps.w0, kc * GR_KC, wrow,
-                           &raw_full[r], pol);
-                ++issued;
+                    bulk_g2s_keep(tbuf + p * GR_BN * nsc, (p ? a.s1 : a.s0) + (int64_t)wrow * nsc, GR_BN * nsc,
+                                  &tile_full[tb]);
+                bulk_g2s_keep(tbuf + NB * GR_BN * nsc, a.sorted + (int64_t)blk * GR_BM, GR_BM * 4, &tile_full[tb]);
+                for (int kc = 0; kc < NK; ++kc, ++g) {
+                    const int r = g % NR;
+                    if (g >= NR && !mbar_wait_abort(&raw_empty[r], ((g / NR) - 1) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&raw_full[r], NB * 8192);
+#pragma unroll
+                    for (int p = 0; p < NB; ++p)
+                        tma_2d(base + L.raw + (r * NB + p) * 8192, p ? &maps.w1 : &maps.w0, kc * GR_KC, wrow,
+                               &raw_full[r], pol);
+                }
             }
-            // never leave the CTA with a copy in flight
-            for (int j = issued > NR ? issued - NR : 0; j < issued; ++j) mbar_wait(&raw_full[j % NR], (j / NR) & 1);
+            // never leave the CTA with a copy in flight (the last ring stages and tile buffers issued)
+            for (int j = g > NR ? g - NR : 0; j < g; ++j) mbar_wait(&raw_full[j % NR], (j / NR) & 1);
+            for (int j = li > TB ? li - TB : 0; j < li; ++j) mbar_wait(&tile_full[j % TB], (j / TB) & 1);
         }
-    } else if (warp == GR_CW + 1) {
+    } else if (warp == GR_MW) {
         // ---------------- MMA warp ----------------
         if (lane == 0) {
             constexpr uint32_t IDESC = gr_idesc(GR_BM, GR_BN);
-            int kc = 0;
-            for (; kc < NK; ++kc) {
-                const int b = kc & 1;
-                if (!mbar_wait_abort(&bf_full[b], (kc >> 1) & 1, abort)) break;
-                fence_proxy_async();
+            int g = 0;  // chunks issued
+            bool ok = true;
+            for (int li = 0; li < n_my && ok; ++li) {
+                const int ab = li & 1;
+                if (li >= 2 && !mbar_wait_abort(&acc_empty[ab], ((li >> 1) - 1) & 1, abort)) break;
                 tc_fence_after();
-                const uint32_t a0 = smem_addr(base + L.a + b * 16384);
+                const uint32_t acc = tmem + ab * NB * 128;
+                for (int kc = 0; kc < NK; ++kc, ++g) {
+                    const int b = g & 1;
+                    if (!mbar_wait_abort(&bf_full[b], (g >> 1) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_addr(base + L.a + b * 16384);
 #pragma unroll
-                for (int p = 0; p < NB; ++p) {
-                    const uint32_t b0 = smem_addr(base + L.bf + (b * NB + p) * 16384);
+                    for (int p = 0; p < NB; ++p) {
+                        const uint32_t b0 = smem_addr(base + L.bf + (b * NB + p) * 16384);
 #pragma unroll
-                    for (int kk = 0; kk < GR_KC / 16; ++kk)
-                        umma_bf16(tmem + p * 128, umma_desc_sw128(a0 + kk * 32), umma_desc_sw128(b0 + kk * 32),
-                                  IDESC, (kc > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < GR_KC / 16; ++kk)
+                            umma_bf16(acc + p * 128, umma_desc_sw128(a0 + kk * 32), umma_desc_sw128(b0 + kk * 32),
+                                      IDESC, (kc > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&bf_empty[b]);
                 }
-                umma_commit(&bf_empty[b]);
+                if (ok) umma_commit(&acc_full[ab]);
             }
-            if (kc == NK)
-                umma_commit(acc_full);
-            else if (kc > 0)  // gave up: let the MMAs already issued finish before TMEM is freed
-                mbar_wait(&bf_empty[(kc - 1) & 1], ((kc - 1) >> 1) & 1);
+            // let the MMAs already issued finish before TMEM is freed
+            if (g > 0) mbar_wait(&bf_empty[(g - 1) & 1], ((g - 1) >> 1) & 1);
         }
-    } else {
+    } else if (warp < GR_CW) {
         // ---------------- consumers: A rows + dequantisation ----------------
         const int ct = tid;  // 0 .. GR_CW*32-1
-        for (int kc = 0; kc < NK; ++kc) {
-            const int b = kc & 1, r = kc % NR;
-            // the MMAs that read stage b two chunks ago must be done
-            if (kc >= 2 && !__all_sync(FULL_MASK, mbar_wait_abort(&bf_empty[b], ((kc >> 1) - 1) & 1, abort))) break;
-            unsigned char* As = base + L.a + b * 16384;
-            const int64_t rs = NB == 2 ? a.d : a.I;  // A row stride in elements
-            for (int q = ct; q < nreal * 8; q += GR_CW * 32) {
-                const int row = q >> 3, c = q & 7;
-                cp_async_16_plain(As + swz128(row, c), a.a_src + (int64_t)tok[row] * rs + kc * GR_KC + c * 8);
-            }
-            cp_async_commit();
-            if (!__all_sync(FULL_MASK, mbar_wait_abort(&raw_full[r], (kc / NR) & 1, abort))) break;
+        int g = 0;
+        bool ok = true;
+        for (int li = 0; li < n_my && ok; ++li) {
+            const int t = (int)blockIdx.x + li * (int)gridDim.x;
+            const int blk = t / ntile;
+            const int tb = li % TB;
+            if (!__all_sync(FULL_MASK, mbar_wait_abort(&tile_full[tb], (li / TB) & 1, abort))) break;
+            const unsigned char* tbuf = base + L.tile + tb * L.tile_bytes;
+            const int32_t* srt = reinterpret_cast<const int32_t*>(tbuf + NB * GR_BN * nsc);
+            // this thread's A rows: ct/8 + 32 i, 16-byte piece ct % 8
+            const uint16_t* src[4];
+            int nsrc = 0;
 #pragma unroll
-            for (int p = 0; p < NB; ++p) {
-                const uint8_t* raw = base + L.raw + (r * NB + p) * 8192;
-                char* dst = reinterpret_cast<char*>(base + L.bf + (b * NB + p) * 16384);
-                const uint8_t* sc_row = scales + p * GR_BN * nsc + kc * 2;
-#pragma unroll
-                for (int i = 0; i < GR_BN * 4 / (GR_CW * 32); ++i) {
-                    const int q = ct + i * GR_CW * 32;
-                    const int row = q >> 2, c = q & 3;
-                    const uint4 w4 = *reinterpret_cast<const uint4*>(raw + row * GR_KC + c * 16);
-                    const float sc = e8m0_to_float(sc_row[row * nsc + (c >> 1)]);
-                    uint32_t o[8];
-#pragma unroll
-                    for (int wq = 0; wq < 4; ++wq) {
-                        float2 lo, hi;
-                        e4m3x4_to_float((&w4.x)[wq], lo, hi);
-                        const __nv_bfloat162 b0 = __floats2bfloat162_rn(lo.x * sc, lo.y * sc);
-                        const __nv_bfloat162 b1 = __floats2bfloat162_rn(hi.x * sc, hi.y * sc);
-                        memcpy(&o[wq * 2], &b0, 4);
-                        memcpy(&o[wq * 2 + 1], &b1, 4);
-                    }
-                    *reinterpret_cast<uint4*>(dst + swz128(row, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
-                    *reinterpret_cast<uint4*>(dst + swz128(row, 2 * c + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+            for (int i = 0; i < 4; ++i) {
+                const int row = (ct >> 3) + 32 * i;
+                const int f = srt[row];
+                if (f < pad) {
+                    const int64_t srow = NB == 2 ? (int64_t)(f / a.k) : (int64_t)blk * GR_BM + row;
+                    src[i] = a.a_src + srow * K + (ct & 7) * 8;
+                    nsrc = i + 1;  // real rows are a prefix of the block
                 }
             }
+            for (int kc = 0; kc < NK; ++kc, ++g) {
+                const int b = g & 1, r = g % NR;
+                // the MMAs that read stage b two chunks ago must be done
+                if (g >= 2 && !__all_sync(FULL_MASK, mbar_wait_abort(&bf_empty[b], ((g >> 1) - 1) & 1, abort))) {
+                    ok = false;
+                    break;
+                }
+                unsigned char* As = base + L.a + b * 16384;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (i < nsrc) cp_async_16_plain(As + swz128((ct >> 3) + 32 * i, ct & 7), src[i] + kc * GR_KC);
+                cp_async_commit();
+                if (!__all_sync(FULL_MASK, mbar_wait_abort(&raw_full[r], (g / NR) & 1, abort))) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int p = 0; p < NB; ++p) {
+                    const uint8_t* raw = base + L.raw + (r * NB + p) * 8192;
+                    char* dst = reinterpret_cast<char*>(base + L.bf + (b * NB + p) * 16384);
+                    const uint8_t* sc_row = tbuf + p * GR_BN * nsc + kc * 2;
+#pragma unroll
+                    for (int i = 0; i < GR_BN * 4 / (GR_CW * 32); ++i) {
+                        const int q = ct + i * GR_CW * 32;
+                        const int row = q >> 2, c = q & 3;
+                        const uint4 w4 = *reinterpret_cast<const uint4*>(raw + row * GR_KC + c * 16);
+                        const float sc = e8m0_to_float(sc_row[row * nsc + (c >> 1)]);
+                        uint32_t o[8];
+#pragma unroll
+                        for (int wq = 0; wq < 4; ++wq) {
+                            float2 lo, hi;
+                            e4m3x4_to_float((&w4.x)[wq], lo, hi);
+                            const __nv_bfloat162 b0 = __floats2bfloat162_rn(lo.x * sc, lo.y * sc);
+                            const __nv_bfloat162 b1 = __floats2bfloat162_rn(hi.x * sc, hi.y * sc);
+                            memcpy(&o[wq * 2], &b0, 4);
+                            memcpy(&o[wq * 2 + 1], &b1, 4);
+                        }
+                        *reinterpret_cast<uint4*>(dst + swz128(row, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4*>(dst + swz128(row, 2 * c + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&raw_empty[r]);
+                cp_async_wait<0>();
+                fence_proxy_async();  // this thread's tile writes, before the tensor cores read them
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bf_full[b]);
+            }
+            if (!ok) break;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&raw_empty[r]);
-            cp_async_wait<0>();
-            fence_proxy_async();  // this thread's tile writes, before the tensor cores read them
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bf_full[b]);
+            if (lane == 0) mbar_arrive(&tile_empty[tb]);
         }
-        cp_async_wait<0>();  // no copy still in flight on any exit from the loop
-        // ---------------- epilogue: TMEM -> h (gate/up) or the slots' partial outputs (down) ----------------
-        if (__all_sync(FULL_MASK, mbar_wait_abort(acc_full, 0, abort))) {
+        cp_async_wait<0>();  // no copy still in flight on any exit
+    } else {
+        // ---------------- epilogue warps: TMEM -> h (gate/up) or the slots' partial outputs (down) ----------------
+        const int quad = warp & 3;                        // TMEM lanes 32 quad .. 32 quad + 31
+        const int m = quad * 32 + lane;                   // accumulator row
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        for (int li = 0; li < n_my; ++li) {
+            const int t = (int)blockIdx.x + li * (int)gridDim.x;
+            const int blk = t / ntile, n0 = (t - blk * ntile) * GR_BN;
+            const int tb = li % TB, ab = li & 1;
+            if (!__all_sync(FULL_MASK, mbar_wait_abort(&acc_full[ab], (li >> 1) & 1, abort))) break;
+            if (!__all_sync(FULL_MASK, mbar_wait_abort(&tile_full[tb], (li / TB) & 1, abort))) break;
             tc_fence_after();
-            const int m = (warp & 3) * 32 + lane;            // accumulator row = TMEM lane
-            const int cb = (warp >> 2) * 64;                 // this warp's 64 columns
-            const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+            const int32_t* srt = reinterpret_cast<const int32_t*>(base + L.tile + tb * L.tile_bytes + NB * GR_BN * nsc);
+            const int f = srt[m];
+            const uint32_t acc = tmem + lane_off + ab * NB * 128;
             const int64_t srow = (int64_t)blk * GR_BM + m;
 #pragma unroll 1
-            for (int c0 = cb; c0 < cb + 64; c0 += 32) {
+            for (int c0 = 0; c0 < GR_BN; c0 += 32) {
                 if (NB == 2) {
-                    float g[32], u[32];
-                    tmem_ld32(lane_base + c0, g);
-                    tmem_ld32(lane_base + 128 + c0, u);
-                    if (m < nreal) {
+                    float gv[32], uv[32];
+                    tmem_ld32(acc + c0, gv);
+                    tmem_ld32(acc + 128 + c0, uv);
+                    if (f < pad) {
                         uint32_t o[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float h0 = g[2 * i] / (1.0f + expf(-g[2 * i])) * u[2 * i];
-                            const float h1 = g[2 * i + 1] / (1.0f + expf(-g[2 * i + 1])) * u[2 * i + 1];
+                            const float h0 = gv[2 * i] / (1.0f + expf(-gv[2 * i])) * uv[2 * i];
+                            const float h1 = gv[2 * i + 1] / (1.0f + expf(-gv[2 * i + 1])) * uv[2 * i + 1];
                             const __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
                             memcpy(&o[i], &hb, 4);
                         }
@@ -338,15 +404,20 @@ __global__ void __launch_bounds__(GR_THREADS, NB == 1 ? 2 : 1) grouped_mma_kerne
                     }
                 } else {
                     float v[32];
-                    tmem_ld32(lane_base + c0, v);
-                    if (m < nreal) {
-                        const int64_t f = a.sorted[srow];
-                        float4* dst = reinterpret_cast<float4*>(a.out + f * a.d + n0 + c0);
+                    tmem_ld32(acc + c0, v);
+                    if (f < pad) {
+                        float4* dst = reinterpret_cast<float4*>(a.out + (int64_t)f * a.d + n0 + c0);
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
                             dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                     }
                 }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&acc_empty[ab]);
+                mbar_arrive(&tile_empty[tb]);
             }
         }
     }
@@ -354,43 +425,64 @@ __global__ void __launch_bounds__(GR_THREADS, NB == 1 ? 2 : 1) grouped_mma_kerne
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(NB * 128) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * NB * 128)
+                     : "memory");
     }
     if (tid == 0 && *abort) atomicOr(a.err, MOE_DEVERR_TIMEOUT);
 }
 
 // y[t][o] = bf16( sum_j w[t][j] * out[t*k + j][o] ), j in order; a slot
 // whose expert id is outside [0, E) (never placed by the sort) adds nothing.
+// Four consecutive outputs per thread (d % 4 == 0).
 __global__ void grouped_combine_kernel(const float* __restrict__ out, const float* __restrict__ w,
                                        const int32_t* __restrict__ ids, int T, int k, int E, int d,
                                        uint16_t* __restrict__ y) {
-    const int64_t n = (int64_t)T * d;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t t = i / d, o = i - t * d;
-        float acc = 0.f;
-        for (int j = 0; j < k; ++j)
-            if ((unsigned)ids[t * k + j] < (unsigned)E) acc = fmaf(w[t * k + j], out[(t * k + j) * d + o], acc);
-        y[i] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+    const int64_t n4 = (int64_t)T * d / 4;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i * 4 / d, o = i * 4 - t * d;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            if ((unsigned)ids[t * k + j] >= (unsigned)E) continue;
+            const float wt = w[t * k + j];
+            const float4 v = *reinterpret_cast<const float4*>(out + (t * k + j) * d + o);
+            acc.x = fmaf(wt, v.x, acc.x);
+            acc.y = fmaf(wt, v.y, acc.y);
+            acc.z = fmaf(wt, v.z, acc.z);
+            acc.w = fmaf(wt, v.w, acc.w);
+        }
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 pk;
+        memcpy(&pk.x, &lo, 4);
+        memcpy(&pk.y, &hi, 4);
+        *reinterpret_cast<uint2*>(y + i * 4) = pk;
     }
 }
 
-// Raw-code ring depth: as deep as the shared memory allows, 2 .. GR_MAXR
-// (the down pass keeps two CTAs per SM).
-static int grouped_ring(int NB, int K, int max_smem) {
-    int NR = NB == 2 ? 6 : 4;
-    while (NR > 2 && gr_layout(NB, K, NR).total + 1024 > (uint32_t)max_smem) --NR;
-    return NR;
+// Ring depth NR and per-tile buffers TB for a pass: the deepest ring (up to
+// 6 stages) with two tile buffers that fits `budget` bytes, else with one.
+static bool grouped_plan(int NB, int K, size_t budget, int* NR, int* TB) {
+    for (int tb = 2; tb >= 1; --tb)
+        for (int nr = 6; nr >= 2; --nr)
+            if (gr_layout(NB, K, nr, tb).total + 1024 <= budget) {
+                *NR = nr;
+                *TB = tb;
+                return true;
+            }
+    return false;
 }
 
 template <int NB>
-static cudaError_t launch_grouped_mma(GRArgs a, const GRMaps& maps, int64_t n_blocks, int ntile, int max_smem,
-                                      int dev, cudaStream_t st) {
+static cudaError_t launch_grouped_mma(GRArgs a, const GRMaps& maps, int64_t n_blocks, const DeviceInfo& di, int dev,
+                                      cudaStream_t st) {
     static std::mutex mu;
     static size_t attr[64] = {0};
     const int K = NB == 2 ? a.d : a.I;
-    a.NR = grouped_ring(NB, K, max_smem);
-    const size_t smem = gr_layout(NB, K, a.NR).total + 1024;
-    if (smem > (size_t)max_smem) return cudaErrorInvalidValue;
+    // the down pass keeps two CTAs per SM (half the SM's shared memory each) when it can
+    size_t budget = (size_t)di.max_smem_optin;
+    if (NB == 1 && grouped_plan(NB, K, (size_t)di.smem_per_sm / 2 - 1024, &a.NR, &a.TB))
+        budget = (size_t)di.smem_per_sm / 2 - 1024;
+    if (!grouped_plan(NB, K, budget, &a.NR, &a.TB)) return cudaErrorInvalidValue;
+    const size_t smem = gr_layout(NB, K, a.NR, a.TB).total + 1024;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -401,14 +493,17 @@ static cudaError_t launch_grouped_mma(GRArgs a, const GRMaps& maps, int64_t n_bl
             attr[dev] = smem;
         }
     }
-    grouped_mma_kernel<NB><<<dim3((unsigned)n_blocks, (unsigned)ntile), GR_THREADS, smem, st>>>(a, maps);
+    const int per_sm = (NB == 1 && smem <= (size_t)di.smem_per_sm / 2 - 1024) ? 2 : 1;
+    const int64_t tiles_max = n_blocks * ((NB == 2 ? a.I : a.d) / GR_BN);
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles_max, (int64_t)di.sm_count * per_sm));
+    grouped_mma_kernel<NB><<<(unsigned)grid, GR_THREADS, smem, st>>>(a, maps);
     return cudaGetLastError();
 }
 
 bool grouped_shape_ok(int d, int I) { return d % 128 == 0 && I % 128 == 0; }
 
 size_t grouped_smem_bytes(int d, int I) {
-    return std::max(gr_layout(2, d, 2).total, gr_layout(1, I, 2).total) + 1024;
+    return std::max(gr_layout(2, d, 2, 1).total, gr_layout(1, I, 2, 1).total) + 1024;
 }
 
 cudaError_t launch_grouped(const uint16_t* x, int T, int d, const int32_t* ids, const float* w, int k, MXView wg,
@@ -448,16 +543,16 @@ cudaError_t launch_grouped(const uint16_t* x, int T, int d, const int32_t* ids, 
     a.a_src = xa;
     a.s0 = wg.s;
     a.s1 = wu.s;
-    if ((err = launch_grouped_mma<2>(a, m1, ws.n_blocks, I / GR_BN, di.max_smem_optin, dev, st)) != cudaSuccess)
+    if ((err = launch_grouped_mma<2>(a, m1, ws.n_blocks, di, dev, st)) != cudaSuccess)
         return err;
     // only the real rows of h_sorted were written: round those (and harmless pad-row bits) through MXFP8
     if (act_mx && (err = launch_mx_requant(ws.h_sorted, ws.h_sorted, ws.n_sorted, I, st)) != cudaSuccess) return err;
     a.a_src = ws.h_sorted;
     a.s0 = wd.s;
     a.s1 = nullptr;
-    if ((err = launch_grouped_mma<1>(a, m2, ws.n_blocks, d / GR_BN, di.max_smem_optin, dev, st)) != cudaSuccess)
+    if ((err = launch_grouped_mma<1>(a, m2, ws.n_blocks, di, dev, st)) != cudaSuccess)
         return err;
-    const int64_t n = (int64_t)T * d;
+    const int64_t n = (int64_t)T * d / 4;
     const int64_t grid = std::min<int64_t>((n + 255) / 256, (int64_t)di.sm_count * 8);
     grouped_combine_kernel<<<(unsigned)std::max<int64_t>(grid, 1), 256, 0, st>>>(ws.out, w, ids, T, k, E, d, y);
     return cudaGetLastError();
