@@ -44,6 +44,8 @@ constexpr int GR_PW = GR_CW;               // the copy warp
 constexpr int GR_MW = GR_CW + 1;           // the MMA warp
 constexpr int GR_THREADS = (GR_CW + 6) * 32;  // + four epilogue warps (10 .. 13: TMEM lane quadrants 2, 3, 0, 1)
 constexpr int GR_MAXR = 8;                 // deepest ring of raw code stages
+constexpr int GR_AROWS = GR_CW * 32 / 8;   // A rows the consumers copy per pass (8 pieces of 16 B per row)
+constexpr int GR_APASS = (GR_BM + GR_AROWS - 1) / GR_AROWS;
 
 struct GRArgs {
     const uint16_t* a_src;     // gate/up: x [T][d] (rows by token); down: h_sorted [n_sorted][I]
@@ -125,6 +127,21 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 // 16 bytes global -> shared (L2 only).
 __device__ __forceinline__ void cp_async_16_plain(void* smem, const void* gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem)), "l"(gmem) : "memory");
+}
+
+// Real rows of a block: its sorted slots below the pad value form a prefix
+// (the sort pads each expert's run at its end); binary search.
+__device__ __forceinline__ int real_rows(const void* srt_bytes, int pad) {
+    const int32_t* srt = reinterpret_cast<const int32_t*>(srt_bytes);
+    int lo = 0, hi = GR_BM;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (srt[mid] < pad)
+            lo = mid + 1;
+        else
+            hi = mid;
+    }
+    return lo;
 }
 
 // 32 consecutive FP32 columns of this thread's TMEM lane.
@@ -256,13 +273,19 @@ __global__ void __launch_bounds__(GR_THREADS, NB == 1 ? 2 : 1) grouped_mma_kerne
         }
     } else if (warp == GR_MW) {
         // ---------------- MMA warp ----------------
+        // D^T = W_tile x A^T: the weight tile is the MMA's A operand (M = 128
+        // rows in TMEM lanes), the block's slot rows its B operand with N =
+        // the real rows rounded up to 16, so a block with few real slots
+        // costs few tensor-core cycles.
         if (lane == 0) {
-            constexpr uint32_t IDESC = gr_idesc(GR_BM, GR_BN);
             int g = 0;  // chunks issued
             bool ok = true;
             for (int li = 0; li < n_my && ok; ++li) {
-                const int ab = li & 1;
+                const int ab = li & 1, tb = li % TB;
                 if (li >= 2 && !mbar_wait_abort(&acc_empty[ab], ((li >> 1) - 1) & 1, abort)) break;
+                if (!mbar_wait_abort(&tile_full[tb], (li / TB) & 1, abort)) break;
+                const int nreal = real_rows(base + L.tile + tb * L.tile_bytes + NB * GR_BN * nsc, pad);
+                const uint32_t idesc = gr_idesc(GR_BN, max(16, (nreal + 15) & ~15));
                 tc_fence_after();
                 const uint32_t acc = tmem + ab * NB * 128;
                 for (int kc = 0; kc < NK; ++kc, ++g) {
@@ -278,8 +301,8 @@ __global__ void __launch_bounds__(GR_THREADS, NB == 1 ? 2 : 1) grouped_mma_kerne
                         const uint32_t b0 = smem_addr(base + L.bf + (b * NB + p) * 16384);
 #pragma unroll
                         for (int kk = 0; kk < GR_KC / 16; ++kk)
-                            umma_bf16(acc + p * 128, umma_desc_sw128(a0 + kk * 32), umma_desc_sw128(b0 + kk * 32),
-                                      IDESC, (kc > 0 || kk > 0) ? 1u : 0u);
+                            umma_bf16(acc + p * 128, umma_desc_sw128(b0 + kk * 32), umma_desc_sw128(a0 + kk * 32),
+                                      idesc, (kc > 0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(&bf_empty[b]);
                 }
@@ -300,13 +323,13 @@ __global__ void __launch_bounds__(GR_THREADS, NB == 1 ? 2 : 1) grouped_mma_kerne
             if (!__all_sync(FULL_MASK, mbar_wait_abort(&tile_full[tb], (li / TB) & 1, abort))) break;
             const unsigned char* tbuf = base + L.tile + tb * L.tile_bytes;
             const int32_t* srt = reinterpret_cast<const int32_t*>(tbuf + NB * GR_BN * nsc);
-            // this thread's A rows: ct/8 + 32 i, 16-byte piece ct % 8
-            const uint16_t* src[4];
+            // this thread's A rows: ct/8 + GR_AROWS i, 16-byte piece ct % 8
+            const uint16_t* src[GR_APASS];
             int nsrc = 0;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int row = (ct >> 3) + 32 * i;
-                const int f = srt[row];
+            for (int i = 0; i < GR_APASS; ++i) {
+                const int row = (ct >> 3) + GR_AROWS * i;
+                const int f = row < GR_BM ? srt[row] : pad;
                 if (f < pad) {
                     const int64_t srow = NB == 2 ? (int64_t)(f / a.k) : (int64_t)blk * GR_BM + row;
                     src[i] = a.a_src + srow * K + (ct & 7) * 8;
@@ -322,8 +345,8 @@ __global__ void __launch_bounds__(GR_THREADS, NB == 1 ? 2 : 1) grouped_mma_kerne
                 }
                 unsigned char* As = base + L.a + b * 16384;
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if (i < nsrc) cp_async_16_plain(As + swz128((ct >> 3) + 32 * i, ct & 7), src[i] + kc * GR_KC);
+                for (int i = 0; i < GR_APASS; ++i)
+                    if (i < nsrc) cp_async_16_plain(As + swz128((ct >> 3) + GR_AROWS * i, ct & 7), src[i] + kc * GR_KC);
                 cp_async_commit();
                 if (!__all_sync(FULL_MASK, mbar_wait_abort(&raw_full[r], (g / NR) & 1, abort))) {
                     ok = false;
@@ -335,8 +358,9 @@ __global__ void __launch_bounds__(GR_THREADS, NB == 1 ? 2 : 1) grouped_mma_kerne
                     char* dst = reinterpret_cast<char*>(base + L.bf + (b * NB + p) * 16384);
                     const uint8_t* sc_row = tbuf + p * GR_BN * nsc + kc * 2;
 #pragma unroll
-                    for (int i = 0; i < GR_BN * 4 / (GR_CW * 32); ++i) {
+                    for (int i = 0; i < (GR_BN * 4 + GR_CW * 32 - 1) / (GR_CW * 32); ++i) {
                         const int q = ct + i * GR_CW * 32;
+                        if (q >= GR_BN * 4) break;
                         const int row = q >> 2, c = q & 3;
                         const uint4 w4 = *reinterpret_cast<const uint4*>(raw + row * GR_KC + c * 16);
                         const float sc = e8m0_to_float(sc_row[row * nsc + (c >> 1)]);
@@ -368,8 +392,9 @@ __global__ void __launch_bounds__(GR_THREADS, NB == 1 ? 2 : 1) grouped_mma_kerne
         cp_async_wait<0>();  // no copy still in flight on any exit
     } else {
         // ---------------- epilogue warps: TMEM -> h (gate/up) or the slots' partial outputs (down) ----------------
+        // TMEM lane = weight row n of the tile, column = slot row m of the block.
         const int quad = warp & 3;                        // TMEM lanes 32 quad .. 32 quad + 31
-        const int m = quad * 32 + lane;                   // accumulator row
+        const int n = quad * 32 + lane;                   // weight row within the tile
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         for (int li = 0; li < n_my; ++li) {
             const int t = (int)blockIdx.x + li * (int)gridDim.x;
@@ -379,38 +404,27 @@ __global__ void __launch_bounds__(GR_THREADS, NB == 1 ? 2 : 1) grouped_mma_kerne
             if (!__all_sync(FULL_MASK, mbar_wait_abort(&tile_full[tb], (li / TB) & 1, abort))) break;
             tc_fence_after();
             const int32_t* srt = reinterpret_cast<const int32_t*>(base + L.tile + tb * L.tile_bytes + NB * GR_BN * nsc);
-            const int f = srt[m];
+            const int nreal = real_rows(srt, pad);
             const uint32_t acc = tmem + lane_off + ab * NB * 128;
-            const int64_t srow = (int64_t)blk * GR_BM + m;
 #pragma unroll 1
-            for (int c0 = 0; c0 < GR_BN; c0 += 32) {
+            for (int c0 = 0; c0 < nreal; c0 += 32) {
                 if (NB == 2) {
                     float gv[32], uv[32];
                     tmem_ld32(acc + c0, gv);
                     tmem_ld32(acc + 128 + c0, uv);
-                    if (f < pad) {
-                        uint32_t o[16];
+                    uint16_t* hp = a.h_sorted + ((int64_t)blk * GR_BM + c0) * a.I + n0 + n;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float h0 = gv[2 * i] / (1.0f + expf(-gv[2 * i])) * uv[2 * i];
-                            const float h1 = gv[2 * i + 1] / (1.0f + expf(-gv[2 * i + 1])) * uv[2 * i + 1];
-                            const __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
-                            memcpy(&o[i], &hb, 4);
+                    for (int i = 0; i < 32; ++i)
+                        if (c0 + i < nreal) {
+                            const float hv = gv[i] / (1.0f + expf(-gv[i])) * uv[i];
+                            hp[(int64_t)i * a.I] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
                         }
-                        uint4* dst = reinterpret_cast<uint4*>(a.h_sorted + srow * a.I + n0 + c0);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-                    }
                 } else {
                     float v[32];
                     tmem_ld32(acc + c0, v);
-                    if (f < pad) {
-                        float4* dst = reinterpret_cast<float4*>(a.out + (int64_t)f * a.d + n0 + c0);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                    }
+                    for (int i = 0; i < 32; ++i)
+                        if (c0 + i < nreal) a.out[(int64_t)srt[c0 + i] * a.d + n0 + n] = v[i];
                 }
             }
             tc_fence_before();
