@@ -39,12 +39,17 @@ namespace moedec {
 constexpr int GR_BM = GROUPED_BLOCK;       // sorted slots per block (the MMA's M)
 constexpr int GR_BN = 128;                 // weight rows per tile (the MMA's N)
 constexpr int GR_KC = 64;                  // K elements per chunk (one 128-byte swizzle row of BF16)
+constexpr int GR_RC = 128;                 // K elements per raw-code stage (two chunks: 128 B per row)
+constexpr int GR_RAW = GR_BN * GR_RC;      // raw-code bytes per matrix and stage
 constexpr int GR_CW = 8;                   // dequantising (consumer) warps: 0 .. 7
 constexpr int GR_PW = GR_CW;               // the copy warp
 constexpr int GR_MW = GR_CW + 1;           // the MMA warp
 constexpr int GR_THREADS = (GR_CW + 6) * 32;  // + four epilogue warps (10 .. 13: TMEM lane quadrants 2, 3, 0, 1)
 constexpr int GR_MAXR = 8;                 // deepest ring of raw code stages
 constexpr int GR_AROWS = GR_CW * 32 / 8;   // A rows the consumers copy per pass (8 pieces of 16 B per row)
+constexpr int GR_IROWS = GR_CW * 32 / 4;   // weight rows the consumers dequantise per pass (4 items per row)
+constexpr int GR_ITEMS = GR_BN / GR_IROWS; // dequantisation items per thread and matrix
+static_assert(GR_BN % GR_IROWS == 0, "whole passes of items");
 constexpr int GR_APASS = (GR_BM + GR_AROWS - 1) / GR_AROWS;
 
 struct GRArgs {
@@ -76,7 +81,7 @@ __host__ __device__ inline GRLayout gr_layout(int NB, int K, int NR, int TB) {
     uint32_t off = 0;
     L.a = off;          off += 2 * 16384;                              // A tile per BF16 stage
     L.bf = off;         off += 2 * NB * 16384;                         // dequantised B tiles
-    L.raw = off;        off += NR * NB * 8192;                         // raw E4M3 codes (TMA ring)
+    L.raw = off;        off += NR * NB * GR_RAW;                       // raw E4M3 codes (TMA ring)
     L.tile_bytes = NB * GR_BN * (K / 32) + GR_BM * 4;                  // a tile's scales + sorted rows
     L.tile = off;       off += TB * L.tile_bytes;
     L.bars = off;       off += (2 * GR_MAXR + 12) * 8;
@@ -165,8 +170,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 // NB = 2: the gate/up GEMMs (K = d, N over I); NB = 1: the down GEMM (K = I,
 // N over d).  Roles, all overlapped across tiles:
 //   copy warp      per tile: the tile's scale rows and sorted slots (1D bulk
-//                  copies); per K chunk: the raw codes (2D TMA) into an
-//                  NR-stage ring;
+//                  copies); per 128 K elements (two chunks): the raw codes
+//                  (2D TMA, 128-byte swizzled rows) into an NR-stage ring;
 //   warps 0..7     per chunk: the real rows of A (cp.async into the 128-byte
 //                  swizzle) and the dequantisation of the codes into BF16
 //                  tiles (two stages);
@@ -239,7 +244,7 @@ __global__ void __launch_bounds__(GR_THREADS, NB == 1 ? 2 : 1) grouped_mma_kerne
         // ---------------- copy warp ----------------
         if (lane == 0) {
             const uint64_t pol = l2_evict_first_policy();
-            int g = 0, li = 0;  // chunks and tiles issued
+            int g = 0, li = 0;  // raw stages and tiles issued
             bool ok = true;
             for (; li < n_my && ok; ++li) {
                 const int t = (int)blockIdx.x + li * (int)gridDim.x;
@@ -254,16 +259,16 @@ __global__ void __launch_bounds__(GR_THREADS, NB == 1 ? 2 : 1) grouped_mma_kerne
                     bulk_g2s_keep(tbuf + p * GR_BN * nsc, (p ? a.s1 : a.s0) + (int64_t)wrow * nsc, GR_BN * nsc,
                                   &tile_full[tb]);
                 bulk_g2s_keep(tbuf + NB * GR_BN * nsc, a.sorted + (int64_t)blk * GR_BM, GR_BM * 4, &tile_full[tb]);
-                for (int kc = 0; kc < NK; ++kc, ++g) {
+                for (int kr = 0; kr < K / GR_RC; ++kr, ++g) {
                     const int r = g % NR;
                     if (g >= NR && !mbar_wait_abort(&raw_empty[r], ((g / NR) - 1) & 1, abort)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&raw_full[r], NB * 8192);
+                    mbar_arrive_expect_tx(&raw_full[r], NB * GR_RAW);
 #pragma unroll
                     for (int p = 0; p < NB; ++p)
-                        tma_2d(base + L.raw + (r * NB + p) * 8192, p ? &maps.w1 : &maps.w0, kc * GR_KC, wrow,
+                        tma_2d(base + L.raw + (r * NB + p) * GR_RAW, p ? &maps.w1 : &maps.w0, kr * GR_RC, wrow,
                                &raw_full[r], pol);
                 }
             }
@@ -314,6 +319,11 @@ __global__ void __launch_bounds__(GR_THREADS, NB == 1 ? 2 : 1) grouped_mma_kerne
     } else if (warp < GR_CW) {
         // ---------------- consumers: A rows + dequantisation ----------------
         const int ct = tid;  // 0 .. GR_CW*32-1
+        // this thread's dequantisation items: rows row0 + GR_IROWS i, 16 codes at c * 16 of each 64-code half
+        const int row0 = ct >> 2, c = ct & 3, sw = row0 & 7;
+        const uint32_t raw_off0 = row0 * 128 + ((c ^ sw) << 4), raw_off1 = row0 * 128 + (((4 + c) ^ sw) << 4);
+        const uint32_t dst_off0 = row0 * 128 + (((2 * c) ^ sw) << 4), dst_off1 = row0 * 128 + (((2 * c + 1) ^ sw) << 4);
+        const int sc_off = row0 * nsc + (c >> 1);
         int g = 0;
         bool ok = true;
         for (int li = 0; li < n_my && ok; ++li) {
@@ -337,7 +347,7 @@ __global__ void __launch_bounds__(GR_THREADS, NB == 1 ? 2 : 1) grouped_mma_kerne
                 }
             }
             for (int kc = 0; kc < NK; ++kc, ++g) {
-                const int b = g & 1, r = g % NR;
+                const int b = g & 1, r = (g >> 1) % NR;  // two chunks per raw stage
                 // the MMAs that read stage b two chunks ago must be done
                 if (g >= 2 && !__all_sync(FULL_MASK, mbar_wait_abort(&bf_empty[b], ((g >> 1) - 1) & 1, abort))) {
                     ok = false;
@@ -348,38 +358,38 @@ __global__ void __launch_bounds__(GR_THREADS, NB == 1 ? 2 : 1) grouped_mma_kerne
                 for (int i = 0; i < GR_APASS; ++i)
                     if (i < nsrc) cp_async_16_plain(As + swz128((ct >> 3) + GR_AROWS * i, ct & 7), src[i] + kc * GR_KC);
                 cp_async_commit();
-                if (!__all_sync(FULL_MASK, mbar_wait_abort(&raw_full[r], (g / NR) & 1, abort))) {
+                if (!__all_sync(FULL_MASK, mbar_wait_abort(&raw_full[r], ((g >> 1) / NR) & 1, abort))) {
                     ok = false;
                     break;
                 }
 #pragma unroll
                 for (int p = 0; p < NB; ++p) {
-                    const uint8_t* raw = base + L.raw + (r * NB + p) * 8192;
+                    const uint8_t* raw = base + L.raw + (r * NB + p) * GR_RAW + ((g & 1) ? raw_off1 : raw_off0);  // swizzled rows
                     char* dst = reinterpret_cast<char*>(base + L.bf + (b * NB + p) * 16384);
-                    const uint8_t* sc_row = tbuf + p * GR_BN * nsc + kc * 2;
+                    const uint8_t* scp = tbuf + p * GR_BN * nsc + sc_off + kc * 2;
 #pragma unroll
-                    for (int i = 0; i < (GR_BN * 4 + GR_CW * 32 - 1) / (GR_CW * 32); ++i) {
-                        const int q = ct + i * GR_CW * 32;
-                        if (q >= GR_BN * 4) break;
-                        const int row = q >> 2, c = q & 3;
-                        const uint4 w4 = *reinterpret_cast<const uint4*>(raw + row * GR_KC + c * 16);
-                        const float sc = e8m0_to_float(sc_row[row * nsc + (c >> 1)]);
+                    for (int i = 0; i < GR_ITEMS; ++i) {  // rows row0 + GR_IROWS * i
+                        const uint4 w4 = *reinterpret_cast<const uint4*>(raw + i * GR_IROWS * 128);
+                        const float sc = e8m0_to_float(scp[i * GR_IROWS * nsc]);
                         uint32_t o[8];
 #pragma unroll
                         for (int wq = 0; wq < 4; ++wq) {
                             float2 lo, hi;
                             e4m3x4_to_float((&w4.x)[wq], lo, hi);
-                            const __nv_bfloat162 b0 = __floats2bfloat162_rn(lo.x * sc, lo.y * sc);
-                            const __nv_bfloat162 b1 = __floats2bfloat162_rn(hi.x * sc, hi.y * sc);
+                            lo = __fmul2_rn(lo, make_float2(sc, sc));
+                            hi = __fmul2_rn(hi, make_float2(sc, sc));
+                            const __nv_bfloat162 b0 = __floats2bfloat162_rn(lo.x, lo.y);
+                            const __nv_bfloat162 b1 = __floats2bfloat162_rn(hi.x, hi.y);
                             memcpy(&o[wq * 2], &b0, 4);
                             memcpy(&o[wq * 2 + 1], &b1, 4);
                         }
-                        *reinterpret_cast<uint4*>(dst + swz128(row, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
-                        *reinterpret_cast<uint4*>(dst + swz128(row, 2 * c + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+                        char* d = dst + i * GR_IROWS * 128;
+                        *reinterpret_cast<uint4*>(d + dst_off0) = make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4*>(d + dst_off1) = make_uint4(o[4], o[5], o[6], o[7]);
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&raw_empty[r]);
+                if (lane == 0 && (g & 1)) mbar_arrive(&raw_empty[r]);  // both chunks of the stage read
                 cp_async_wait<0>();
                 fence_proxy_async();  // this thread's tile writes, before the tensor cores read them
                 __syncwarp();
@@ -473,10 +483,11 @@ __global__ void grouped_combine_kernel(const float* __restrict__ out, const floa
 }
 
 // Ring depth NR and per-tile buffers TB for a pass: the deepest ring (up to
-// 6 stages) with two tile buffers that fits `budget` bytes, else with one.
+// 4 stages of 128 K elements) with two tile buffers that fits `budget`
+// bytes, else with one.
 static bool grouped_plan(int NB, int K, size_t budget, int* NR, int* TB) {
     for (int tb = 2; tb >= 1; --tb)
-        for (int nr = 6; nr >= 2; --nr)
+        for (int nr = 4; nr >= 2; --nr)
             if (gr_layout(NB, K, nr, tb).total + 1024 <= budget) {
                 *NR = nr;
                 *TB = tb;
@@ -529,9 +540,9 @@ cudaError_t launch_grouped(const uint16_t* x, int T, int d, const int32_t* ids, 
     int dev = 0;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
     GRMaps m1{}, m2{};
-    if (!map_2d_u8(&m1.w0, wg.w, (uint64_t)E * I, d, GR_BN, GR_KC) ||
-        !map_2d_u8(&m1.w1, wu.w, (uint64_t)E * I, d, GR_BN, GR_KC) ||
-        !map_2d_u8(&m2.w0, wd.w, (uint64_t)E * d, I, GR_BN, GR_KC))
+    if (!map_2d_u8(&m1.w0, wg.w, (uint64_t)E * I, d, GR_BN, GR_RC, true) ||
+        !map_2d_u8(&m1.w1, wu.w, (uint64_t)E * I, d, GR_BN, GR_RC, true) ||
+        !map_2d_u8(&m2.w0, wd.w, (uint64_t)E * d, I, GR_BN, GR_RC, true))
         return cudaErrorInvalidValue;
     m2.w1 = m2.w0;
     err = launch_align(ids, T, k, E, GR_BM, ws.sorted, ws.n_sorted, ws.expert_ids, ws.n_blocks, ws.ntpp, ws.align_ws,
