@@ -136,139 +136,188 @@ __device__ inline void build_route_map(const RouteMap& m, const int32_t* __restr
     const int PT = min((int)blockDim.x, DEC_THREADS) & ~31, PW = PT >> 5;
     const bool part = tid < PT;
     const int n = s.B * s.k;
-    // Parallel placement (32 < n <= PT, with a PW x E scratch table, e.g. the
-    // idle copy ring; one warp's worth of slots is placed as fast serially):
-    // thread f holds slot f; its position inside its expert's
-    // range is the number of earlier slots with the same expert, i.e. the
-    // slots of earlier warps (per-warp counts, scanned over warps) plus the
-    // earlier lanes of its own warp (a match mask).
-    const bool fast = n > 32 && n <= PT && scratch != nullptr && scratch_ints >= s.E * PW;
-    int my_e = -1, my_rank = 0;
-    float my_w = 0.f;
-    if (fast) {
-        if (tid < n) {
-            my_e = ids[tid];
-            if (w) my_w = w[tid];
-        }
-        for (int i = tid; i < s.E * PW; i += blockDim.x) scratch[i] = 0;
-        if (tid < n && (unsigned)my_e >= (unsigned)s.E) {
-            my_e = -1;
-            atomicOr(err, MOE_DEVERR_EXPERT_ID);
-        }
-        __syncthreads();
-        if (part) {
-            const unsigned mask = __match_any_sync(FULL_MASK, my_e);
-            my_rank = __popc(mask & lanemask_lt());
-            if (my_e >= 0 && my_rank == 0) scratch[my_e * PW + warp] = __popc(mask);
-        }
-        __syncthreads();
-        // per expert: counts of the earlier warps (exclusive) and the total
-        if (part)
-            for (int e = tid; e < s.E; e += PT) {
-                int c = 0;
-                for (int q = 0; q < PW; ++q) {
-                    const int t = scratch[e * PW + q];
-                    scratch[e * PW + q] = c;
-                    c += t;
-                }
-                m.cnt[e] = c;
-            }
-    } else {
-        if (part)
-            for (int e = tid; e < s.E; e += PT) m.cnt[e] = 0;
-        __syncthreads();
-        if (part) {
-            int bad = 0;
-            for (int f = tid; f < n; f += PT) {
-                int e = ids[f];
-                if ((unsigned)e < (unsigned)s.E) {
-                    atomicAdd(&m.cnt[e], 1);
-                } else {
+    const int KS = s.k + s.S;
+    if (n <= 32) {
+        // Few slots (B * k <= 32): one warp builds the map.  A slot's expert
+        // group is its __match_any_sync mask; the distinct experts are
+        // numbered, and their slot ranges laid out, in increasing expert id
+        // (as the general path does), slots inside a range in flat order.
+        if (warp == 0) {
+            int e = -1;
+            float wv = 0.f;
+            if (lane < n) {
+                e = ids[lane];
+                if (w) wv = w[lane];
+                if ((unsigned)e >= (unsigned)s.E) {
                     e = -1;
-                    bad = 1;
+                    atomicOr(err, MOE_DEVERR_EXPERT_ID);
                 }
-                m.sid[f] = e;
             }
-            if (bad) atomicOr(err, MOE_DEVERR_EXPERT_ID);
-        }
-    }
-    __syncthreads();
-
-    // Exclusive scan over experts of (count << 16 | present): gives each
-    // present expert its distinct index (low half) and slot offset (high).
-    const int per = (s.E + PT - 1) / PT;
-    const int e0 = part ? min(tid * per, s.E) : s.E, e1 = part ? min(e0 + per, s.E) : s.E;
-    int local = 0, incl = 0;
-    if (part) {
-        for (int e = e0; e < e1; ++e) {
-            const int c = m.cnt[e];
-            local += (c << 16) | (c > 0 ? 1 : 0);
-        }
-        incl = local;
-        for (int off = 1; off < 32; off <<= 1) {
-            const int v = __shfl_up_sync(FULL_MASK, incl, off);
-            if (lane >= off) incl += v;
-        }
-        if (lane == 31) m.wtot[warp] = incl;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        const int v = lane < PW ? m.wtot[lane] : 0;
-        int sc = v;
-        for (int off = 1; off < 32; off <<= 1) {
-            const int t = __shfl_up_sync(FULL_MASK, sc, off);
-            if (lane >= off) sc += t;
-        }
-        if (lane < PW) m.wtot[lane] = sc - v;
-        if (lane == PW - 1) {
-            m.hdr[1] = sc & 0xffff;
-            m.hdr[2] = sc >> 16;
-        }
-    }
-    __syncthreads();
-    if (part) {
-        int run = m.wtot[warp] + incl - local;
-        for (int e = e0; e < e1; ++e) {
-            const int c = m.cnt[e];
-            if (c > 0) {
-                const int uid = run & 0xffff, off = run >> 16;
+            const unsigned grp = __match_any_sync(FULL_MASK, e);
+            const unsigned below = grp & lanemask_lt();
+            const bool lead = e >= 0 && below == 0;
+            const int cnt = __popc(grp);
+            const unsigned leaders = __ballot_sync(FULL_MASK, lead);
+            int uid = 0, off = 0;  // distinct experts with a smaller id and their slots
+            for (unsigned rest = leaders; rest; rest &= rest - 1) {
+                const int q = __ffs(rest) - 1;
+                const int eq = __shfl_sync(FULL_MASK, e, q), cq = __shfl_sync(FULL_MASK, cnt, q);
+                if (e >= 0 && eq < e) {
+                    ++uid;
+                    off += cq;
+                }
+            }
+            if (lead) {
                 m.uexp[uid] = e;
                 m.uoff[uid] = off;
-                m.cnt[e] = off;
-                run += (c << 16) | 1;
             }
-        }
-    }
-    __syncthreads();
-
-    // Stable placement of slots into their expert's range (the order inside
-    // an expert is increasing flat slot index).
-    const int nu = m.hdr[1], tot = m.hdr[2];
-    const int KS = s.k + s.S;
-    if (fast) {
-        if (my_e >= 0) {
-            const int pos = m.cnt[my_e] + scratch[my_e * PW + warp] + my_rank;
-            const int b = tid / s.k, j = tid - b * s.k;
-            m.hrow[pos] = b * KS + j;
-            if (m.wt) m.wt[pos] = my_w;
-        }
-    } else if (warp == 0) {
-        for (int f0 = 0; f0 < n; f0 += 32) {
-            const int f = f0 + lane;
-            const int e = f < n ? m.sid[f] : -1;
-            const unsigned grp = __match_any_sync(FULL_MASK, e);
-            const int base = e >= 0 ? m.cnt[e] : 0;
-            __syncwarp();
             if (e >= 0) {
-                const int pos = base + __popc(grp & lanemask_lt());
-                const int b = f / s.k, j = f - b * s.k;
+                const int pos = off + __popc(below);
+                const int b = lane / s.k, j = lane - b * s.k;
                 m.hrow[pos] = b * KS + j;
-                if (m.wt) m.wt[pos] = w[f];
-                if ((grp & lanemask_lt()) == 0) m.cnt[e] = base + __popc(grp);
+                if (m.wt) m.wt[pos] = wv;
             }
-            __syncwarp();
+            const int tot_r = __popc(__ballot_sync(FULL_MASK, e >= 0));
+            if (lane == 0) {
+                m.hdr[1] = __popc(leaders);
+                m.hdr[2] = tot_r;
+            }
+        }
+        __syncthreads();
+    } else {
+        // Parallel placement (32 < n <= PT, with a PW x E scratch table, e.g. the
+        // idle copy ring; one warp's worth of slots is placed as fast serially):
+        // thread f holds slot f; its position inside its expert's
+        // range is the number of earlier slots with the same expert, i.e. the
+        // slots of earlier warps (per-warp counts, scanned over warps) plus the
+        // earlier lanes of its own warp (a match mask).
+        const bool fast = n > 32 && n <= PT && scratch != nullptr && scratch_ints >= s.E * PW;
+        int my_e = -1, my_rank = 0;
+        float my_w = 0.f;
+        if (fast) {
+            if (tid < n) {
+                my_e = ids[tid];
+                if (w) my_w = w[tid];
+            }
+            for (int i = tid; i < s.E * PW; i += blockDim.x) scratch[i] = 0;
+            if (tid < n && (unsigned)my_e >= (unsigned)s.E) {
+                my_e = -1;
+                atomicOr(err, MOE_DEVERR_EXPERT_ID);
+            }
+            __syncthreads();
+            if (part) {
+                const unsigned mask = __match_any_sync(FULL_MASK, my_e);
+                my_rank = __popc(mask & lanemask_lt());
+                if (my_e >= 0 && my_rank == 0) scratch[my_e * PW + warp] = __popc(mask);
+            }
+            __syncthreads();
+            // per expert: counts of the earlier warps (exclusive) and the total
+            if (part)
+                for (int e = tid; e < s.E; e += PT) {
+                    int c = 0;
+                    for (int q = 0; q < PW; ++q) {
+                        const int t = scratch[e * PW + q];
+                        scratch[e * PW + q] = c;
+                        c += t;
+                    }
+                    m.cnt[e] = c;
+                }
+        } else {
+            if (part)
+                for (int e = tid; e < s.E; e += PT) m.cnt[e] = 0;
+            __syncthreads();
+            if (part) {
+                int bad = 0;
+                for (int f = tid; f < n; f += PT) {
+                    int e = ids[f];
+                    if ((unsigned)e < (unsigned)s.E) {
+                        atomicAdd(&m.cnt[e], 1);
+                    } else {
+                        e = -1;
+                        bad = 1;
+                    }
+                    m.sid[f] = e;
+                }
+                if (bad) atomicOr(err, MOE_DEVERR_EXPERT_ID);
+            }
+        }
+        __syncthreads();
+
+        // Exclusive scan over experts of (count << 16 | present): gives each
+        // present expert its distinct index (low half) and slot offset (high).
+        const int per = (s.E + PT - 1) / PT;
+        const int e0 = part ? min(tid * per, s.E) : s.E, e1 = part ? min(e0 + per, s.E) : s.E;
+        int local = 0, incl = 0;
+        if (part) {
+            for (int e = e0; e < e1; ++e) {
+                const int c = m.cnt[e];
+                local += (c << 16) | (c > 0 ? 1 : 0);
+            }
+            incl = local;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(FULL_MASK, incl, off);
+                if (lane >= off) incl += v;
+            }
+            if (lane == 31) m.wtot[warp] = incl;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const int v = lane < PW ? m.wtot[lane] : 0;
+            int sc = v;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int t = __shfl_up_sync(FULL_MASK, sc, off);
+                if (lane >= off) sc += t;
+            }
+            if (lane < PW) m.wtot[lane] = sc - v;
+            if (lane == PW - 1) {
+                m.hdr[1] = sc & 0xffff;
+                m.hdr[2] = sc >> 16;
+            }
+        }
+        __syncthreads();
+        if (part) {
+            int run = m.wtot[warp] + incl - local;
+            for (int e = e0; e < e1; ++e) {
+                const int c = m.cnt[e];
+                if (c > 0) {
+                    const int uid = run & 0xffff, off = run >> 16;
+                    m.uexp[uid] = e;
+                    m.uoff[uid] = off;
+                    m.cnt[e] = off;
+                    run += (c << 16) | 1;
+                }
+            }
+        }
+        __syncthreads();
+
+        // Stable placement of slots into their expert's range (the order inside
+        // an expert is increasing flat slot index).
+        if (fast) {
+            if (my_e >= 0) {
+                const int pos = m.cnt[my_e] + scratch[my_e * PW + warp] + my_rank;
+                const int b = tid / s.k, j = tid - b * s.k;
+                m.hrow[pos] = b * KS + j;
+                if (m.wt) m.wt[pos] = my_w;
+            }
+        } else if (warp == 0) {
+            for (int f0 = 0; f0 < n; f0 += 32) {
+                const int f = f0 + lane;
+                const int e = f < n ? m.sid[f] : -1;
+                const unsigned grp = __match_any_sync(FULL_MASK, e);
+                const int base = e >= 0 ? m.cnt[e] : 0;
+                __syncwarp();
+                if (e >= 0) {
+                    const int pos = base + __popc(grp & lanemask_lt());
+                    const int b = f / s.k, j = f - b * s.k;
+                    m.hrow[pos] = b * KS + j;
+                    if (m.wt) m.wt[pos] = w[f];
+                    if ((grp & lanemask_lt()) == 0) m.cnt[e] = base + __popc(grp);
+                }
+                __syncwarp();
+            }
         }
     }
+    const int nu = m.hdr[1], tot = m.hdr[2];
     if (tid == 0) {
         m.uoff[nu] = tot;
         m.hdr[0] = nu + s.S;
