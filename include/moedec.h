@@ -137,10 +137,11 @@ int moe_down(const void* h, int B, int k, const int32_t* topk_ids, const float* 
  * the E8M0 scales stay one per 32 elements along K ([E][I][d/32],
  * [E][d][I/32]).  The GC-MoE page names FP8/FP4 MoE operators; MXFP4 halves
  * the weight bytes of MXFP8.  x and h 16-byte aligned, codes 32-byte aligned.
- * One warp computes one output value ([WD, how the two kernels work]);
- * tokens sharing an expert each stream its rows.  An expert id outside
- * [0, E) sets MOE_DEVERR_EXPERT_ID, its h is written as zero and down skips
- * the slot.
+ * For B >= 2 (and d % 512 == 0, I % 256 == 0, 16-byte aligned scales) the
+ * passes run on the same row-tile kernels as MXFP8, each distinct expert's
+ * rows streamed once per call; otherwise one warp computes one output value
+ * ([WD, how the two kernels work]).  An expert id outside [0, E) sets
+ * MOE_DEVERR_EXPERT_ID, its h is written as zero and down skips the slot.
  */
 int moe_gate_up_fp4(const void* x, int B, int d, const int32_t* topk_ids, int k, moe_mx_t w_gate,
                     moe_mx_t w_up, int E, int I, const moe_mx_t* shared_gate,

@@ -129,7 +129,8 @@ __device__ inline RouteMap carve_map(int* p, const DecodeShape& s, bool with_w) 
 
 __device__ inline void build_route_map(const RouteMap& m, const int32_t* __restrict__ ids,
                                 const float* __restrict__ w, const DecodeShape& s, int* err,
-                                bool merge = false, int* scratch = nullptr, int scratch_ints = 0) {
+                                bool merge = false, int* scratch = nullptr, int scratch_ints = 0,
+                                bool small = true) {
     // The first PT = min(blockDim.x, DEC_THREADS) threads (whole warps) build
     // the map; any further threads only take part in the barriers.
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -137,7 +138,7 @@ __device__ inline void build_route_map(const RouteMap& m, const int32_t* __restr
     const bool part = tid < PT;
     const int n = s.B * s.k;
     const int KS = s.k + s.S;
-    if (n <= 32) {
+    if (small && n <= 32) {
         // Few slots (B * k <= 32): one warp builds the map.  A slot's expert
         // group is its __match_any_sync mask; the distinct experts are
         // numbered, and their slot ranges laid out, in increasing expert id

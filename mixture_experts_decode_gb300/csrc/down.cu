@@ -460,8 +460,10 @@ __global__ void __launch_bounds__((CW + 1) * 32, 2) down_v4_kernel(DownArgs a) {
         mbar_init_fence();
     }
     // the copy ring is idle until the map is built: it serves as the map's scratch
+    // (the one-warp map for small B is left out here: in this kernel it
+    // measured slower at B = 32 through register allocation)
     build_route_map(m, a.ids, a.w, s, a.err, true, reinterpret_cast<int*>(ring),
-                    L.S * L.stage_bytes / 4);  // ends with __syncthreads
+                    L.S * L.stage_bytes / 4, false);  // ends with __syncthreads
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = CL > 1 ? (int)cluster_rank() : 0;

@@ -118,6 +118,34 @@ def test_fp4_wide_scale_exponents(cuda_device, E, k, d, I):
     _compare(cuda_device, W, Wd, x, ids, w, range(5), f"fp4 wide scales {E},{k},{d},{I}")
 
 
+@pytest.mark.parametrize("E,k,d,I", [(4, 2, 512, 256), (3, 3, 1056, 64)])
+def test_fp4_scale_exponents_at_the_ends(cuda_device, E, k, d, I):
+    """Some blocks' scale bytes at the bottom of the E8M0 range (1..4: the
+    scaled partial sums are FP32 subnormals or nearly) and some 21..26 above
+    the rest (the block dominates its dot product; larger steps would take y
+    past the FP32 range), on both kernel families:
+    each block's scale multiplies its own partial sum, and the routing weight
+    the expert's whole dot, as the oracle computes them."""
+    cfg = inputs.LayerConfig(f"fp4_ends_{E}_{k}_{d}_{I}", E, k, d, I, True, "softmax_normal")
+    W = inputs.layer_weights(cfg, "cpu", fp4=True)
+    g = torch.Generator().manual_seed(12)
+    def ends(sc):
+        u = torch.rand(sc.shape, generator=g)
+        low = torch.randint(1, 5, sc.shape, generator=g, dtype=torch.int32)
+        high = sc.to(torch.int32) + torch.randint(21, 27, sc.shape, generator=g, dtype=torch.int32)
+        out = torch.where(u < 0.1, low, torch.where(u > 0.95, high.clamp(max=254), sc.to(torch.int32)))
+        return out.to(torch.uint8)
+    for n in ("s_gate", "s_up", "s_down"):
+        W[n] = ends(W[n])
+    sh = list(W["shared"])
+    for i in (1, 3, 5):
+        sh[i] = ends(sh[i])
+    W["shared"] = tuple(sh)
+    Wd = _dev_weights(W, cuda_device)
+    x, ids, w = inputs.layer_batch(cfg, 5)
+    _compare(cuda_device, W, Wd, x, ids, w, range(5), f"fp4 end scales {E},{k},{d},{I}")
+
+
 @pytest.mark.parametrize("E,k,d,I", [(5, 2, 96, 160), (3, 3, 1056, 64)])
 def test_fp4_shared_expert_and_ragged_lanes(cuda_device, E, k, d, I):
     """A shared expert; rows whose chunk count is not a multiple of 32."""
