@@ -9,11 +9,19 @@ in TB/s, where a step's bytes are
     U*3*I*d*33/32 (+ shared) + 2Bd (x) + 8Bk (ids, w) + 4B(k+S)I (h) + 2Bd (y)
 with U the exact number of distinct experts of that step's routing.
 
-Also reported: the same-run copy-kernel peak, per-kernel durations with the
-dominant kernel's roofline, the end-to-end number through moe_layer_host
-(host buffers, copies inside the timed region), align at prefill scale, the
-SM clocks sampled during the timed region and the CPU oracle on a bounded
-sample.  `--impl reference` times the CPU oracle itself on this workload.
+The timed region (K steps in CUDA graphs between CUDA events, barrier and
+synchronize on both sides) is repeated and the median region is reported.
+
+Also reported: the same-run copy-kernel peak, each pass alone with the
+dominant kernel's roofline and the whole layer's fraction, the end-to-end
+number through moe_layer_host (host buffers, copies inside the timed
+region), align at prefill scale for two routings, the router, the MXFP8
+activation round trip, the MXFP4 passes, the expert-centric grouped layer
+against the decode layer from B=32 to 4096, the sweep of every decode
+config (Qwen3 B=1..32, the routing-locality configs, DeepSeek-V3 with its
+shared expert), the SM clocks sampled during the timed region and the CPU
+oracle on a bounded sample.  `--impl reference` times the CPU oracle itself
+on this workload; `--profile` runs a few plain calls of one path for ncu.
 
 N > 1 (torchrun): every rank runs an independent replica (weak scaling).
 """
