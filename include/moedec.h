@@ -204,14 +204,18 @@ int moe_layer_host(const void* x_host, int B, int d, const int32_t* topk_ids_hos
  *   4. if act_mx, h is rounded through MXFP8;
  *   5. out[slot] = h[slot] times deq(Wd[e]) (FP32);
  *   6. y[t,o] = bf16_rn( sum_j topk_w[t,j] * out[t*k+j, o] ), j in order.
- * The sums run in the tensor cores' order, not the decode layer's, so the
- * results agree with moe_layer to FP32 rounding, not bit for bit.  No shared
- * expert.
+ * With a shared expert (all three shared pointers, [1][rows][K] each) steps
+ * 3-5 also run as a one-expert layer over every token in order, and step 6
+ * adds its row with weight 1.0 after the k routed slots.  The sums run in
+ * the tensor cores' order, not the decode layer's, so the results agree with
+ * moe_layer to FP32 rounding, not bit for bit.
  * Arguments
  *   x         BF16 [T][d], 32-byte aligned.  topk_ids int32 [T][k]; an id
  *             outside [0, E) adds nothing and sets MOE_DEVERR_EXPERT_ID.
  *   topk_w    float32 [T][k].  weights as for moe_layer; each scale array
  *             16-byte aligned.
+ *   shared_gate, shared_up, shared_down: NULL for no shared expert, else
+ *             MXFP8 [1][I][d], [1][I][d], [1][d][I] (all three or none).
  *   d, I      multiples of 128.  E <= MOE_ALIGN_MAX_EXPERTS; T*k +
  *             E*127 < 2^31.  No limit on T beyond that.
  *   act_mx    0: activations as given (the decode layer's numerics);
@@ -221,10 +225,11 @@ int moe_layer_host(const void* x_host, int B, int d, const int32_t* topk_ids_hos
  * Errors: MOE_ERR_SHAPE (d or I not a multiple of 128, k > E),
  * MOE_ERR_LIMIT, MOE_ERR_WORKSPACE, MOE_ERR_ALIGN, MOE_ERR_CUDA.
  */
-int moe_layer_grouped_workspace_bytes(int T, int k, int E, int d, int I, size_t* bytes);
+int moe_layer_grouped_workspace_bytes(int T, int k, int E, int d, int I, int has_shared, size_t* bytes);
 int moe_layer_grouped(const void* x, int T, int d, const int32_t* topk_ids, const float* topk_w, int k,
-                      moe_mx_t w_gate, moe_mx_t w_up, moe_mx_t w_down, int E, int I, int act_mx,
-                      void* workspace, size_t workspace_bytes, void* y, moe_stream_t stream);
+                      moe_mx_t w_gate, moe_mx_t w_up, moe_mx_t w_down, int E, int I,
+                      const moe_mx_t* shared_gate, const moe_mx_t* shared_up, const moe_mx_t* shared_down,
+                      int act_mx, void* workspace, size_t workspace_bytes, void* y, moe_stream_t stream);
 
 /*
  * moe_align_sizes -- output and workspace sizes for moe_align_block_size:

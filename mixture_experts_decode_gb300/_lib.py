@@ -79,8 +79,8 @@ def load(path: str = LIB_PATH):
         "moe_align_static_fits": ([I, I, I], I),
         "moe_copy": ([P, P, S, P], I),
         "moe_device_error": ([P, ctypes.POINTER(I)], I),
-        "moe_layer_grouped_workspace_bytes": ([I, I, I, I, I, ctypes.POINTER(S)], I),
-        "moe_layer_grouped": ([P, I, I, P, P, I, MXView, MXView, MXView, I, I, I, P, S, P, P], I),
+        "moe_layer_grouped_workspace_bytes": ([I, I, I, I, I, I, ctypes.POINTER(S)], I),
+        "moe_layer_grouped": ([P, I, I, P, P, I, MXView, MXView, MXView, I, I, MXP, MXP, MXP, I, P, S, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -230,17 +230,18 @@ def layer(x, topk_ids, topk_w, w_gate: MX, w_up: MX, w_down: MX, shared=None,
     return y
 
 
-def layer_grouped_workspace_bytes(T: int, k: int, E: int, d: int, I: int) -> int:
+def layer_grouped_workspace_bytes(T: int, k: int, E: int, d: int, I: int, has_shared: bool = False) -> int:
     out = ctypes.c_size_t()
     _check("moe_layer_grouped_workspace_bytes",
-           load().moe_layer_grouped_workspace_bytes(T, k, E, d, I, ctypes.byref(out)))
+           load().moe_layer_grouped_workspace_bytes(T, k, E, d, I, int(has_shared), ctypes.byref(out)))
     return out.value
 
 
-def layer_grouped(x, topk_ids, topk_w, w_gate: MX, w_up: MX, w_down: MX, act_mx: bool = False,
+def layer_grouped(x, topk_ids, topk_w, w_gate: MX, w_up: MX, w_down: MX, shared=None, act_mx: bool = False,
                   workspace: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None):
     """The layer computed expert-centrically (align, grouped tensor-core GEMMs,
-    combine) on the current stream; act_mx rounds x and h through MXFP8."""
+    combine) on the current stream; act_mx rounds x and h through MXFP8;
+    shared = (gate, up, down) MX triples of a shared expert, or None."""
     lib = load()
     dev = x.device
     _need(x, "x", torch.bfloat16, None, 2)
@@ -251,7 +252,10 @@ def layer_grouped(x, topk_ids, topk_w, w_gate: MX, w_up: MX, w_down: MX, act_mx:
     E, I = w_gate.w.shape[0], w_gate.w.shape[1]
     vg, vu = _mx(w_gate, "w_gate", dev, I, d), _mx(w_up, "w_up", dev, I, d, E)
     vd = _mx(w_down, "w_down", dev, d, I, E)
-    need = layer_grouped_workspace_bytes(T, k, E, d, I)
+    sg, su, sd = _shared3(shared)
+    vsg, vsu, vsd = (_mx(sg, "shared_gate", dev, I, d, 1), _mx(su, "shared_up", dev, I, d, 1),
+                     _mx(sd, "shared_down", dev, d, I, 1))
+    need = layer_grouped_workspace_bytes(T, k, E, d, I, shared is not None)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     _need(workspace, "workspace", torch.uint8, dev)
@@ -259,8 +263,8 @@ def layer_grouped(x, topk_ids, topk_w, w_gate: MX, w_up: MX, w_down: MX, act_mx:
         y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
     _need(y, "y", torch.bfloat16, dev)
     _check("moe_layer_grouped", lib.moe_layer_grouped(
-        x.data_ptr(), T, d, topk_ids.data_ptr(), topk_w.data_ptr(), k, vg, vu, vd, E, I, int(bool(act_mx)),
-        workspace.data_ptr(), workspace.numel(), y.data_ptr(), _stream(dev)))
+        x.data_ptr(), T, d, topk_ids.data_ptr(), topk_w.data_ptr(), k, vg, vu, vd, E, I, _ref(vsg), _ref(vsu),
+        _ref(vsd), int(bool(act_mx)), workspace.data_ptr(), workspace.numel(), y.data_ptr(), _stream(dev)))
     return y
 
 

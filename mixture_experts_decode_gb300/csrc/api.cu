@@ -138,7 +138,7 @@ int down_checked(const void* h, bool h32, int B, int k, const int32_t* ids, cons
 
 // Carves the grouped layer's buffers out of one workspace (256-byte aligned
 // pieces); returns the bytes used.  ws == nullptr only measures.
-size_t grouped_carve(int T, int k, int E, int d, int I, char* base, GroupedWorkspace* ws) {
+size_t grouped_carve(int T, int k, int E, int d, int I, bool shared, char* base, GroupedWorkspace* ws) {
     const int64_t ns = (int64_t)T * k + (int64_t)E * (GROUPED_BLOCK - 1);
     const int64_t nb = (ns + GROUPED_BLOCK - 1) / GROUPED_BLOCK;
     size_t off = 0;
@@ -154,7 +154,19 @@ size_t grouped_carve(int T, int k, int E, int d, int I, char* base, GroupedWorks
     char* xmx = take((size_t)T * d * 2);
     char* hs = take((size_t)ns * I * 2);
     char* out = take((size_t)T * k * d * 4);
+    const int64_t nsh = shared ? ((int64_t)T + GROUPED_BLOCK - 1) / GROUPED_BLOCK * GROUPED_BLOCK : 0;
+    char* sh_sorted = shared ? take((size_t)nsh * 4) : nullptr;
+    char* sh_expert = shared ? take((size_t)nsh / GROUPED_BLOCK * 4) : nullptr;
+    char* sh_ntpp = shared ? take(4) : nullptr;
+    char* sh_h = shared ? take((size_t)nsh * I * 2) : nullptr;
+    char* sh_out = shared ? take((size_t)T * d * 4) : nullptr;
     if (ws) {
+        ws->sh_sorted = reinterpret_cast<int32_t*>(sh_sorted);
+        ws->sh_expert = reinterpret_cast<int32_t*>(sh_expert);
+        ws->sh_ntpp = reinterpret_cast<int32_t*>(sh_ntpp);
+        ws->n_sh = nsh;
+        ws->sh_h = reinterpret_cast<uint16_t*>(sh_h);
+        ws->sh_out = reinterpret_cast<float*>(sh_out);
         ws->sorted = reinterpret_cast<int32_t*>(sorted);
         ws->n_sorted = ns;
         ws->expert_ids = reinterpret_cast<int32_t*>(eids);
@@ -327,26 +339,34 @@ int moe_layer_host(const void* x_host, int B, int d, const int32_t* topk_ids_hos
     return MOE_OK;
 }
 
-int moe_layer_grouped_workspace_bytes(int T, int k, int E, int d, int I, size_t* bytes) {
+int moe_layer_grouped_workspace_bytes(int T, int k, int E, int d, int I, int has_shared, size_t* bytes) {
     if (!bytes) return MOE_ERR_ARG;
     const int rc = check_grouped_shape(T, k, E, d, I);
     if (rc) return rc;
-    *bytes = grouped_carve(T, k, E, d, I, nullptr, nullptr);
+    *bytes = grouped_carve(T, k, E, d, I, has_shared != 0, nullptr, nullptr);
     return MOE_OK;
 }
 
 int moe_layer_grouped(const void* x, int T, int d, const int32_t* topk_ids, const float* topk_w, int k,
-                      moe_mx_t w_gate, moe_mx_t w_up, moe_mx_t w_down, int E, int I, int act_mx,
-                      void* workspace, size_t workspace_bytes, void* y, moe_stream_t stream) {
+                      moe_mx_t w_gate, moe_mx_t w_up, moe_mx_t w_down, int E, int I,
+                      const moe_mx_t* shared_gate, const moe_mx_t* shared_up, const moe_mx_t* shared_down,
+                      int act_mx, void* workspace, size_t workspace_bytes, void* y, moe_stream_t stream) {
     int rc = check_grouped_shape(T, k, E, d, I);
     if (rc) return rc;
     if (act_mx != 0 && act_mx != 1) return MOE_ERR_ARG;
+    const int ns = (shared_gate != nullptr) + (shared_up != nullptr) + (shared_down != nullptr);
+    if (ns != 0 && ns != 3) return MOE_ERR_ARG;
     if (T == 0) return MOE_OK;
     if (!x || !topk_ids || !topk_w || !y) return MOE_ERR_ARG;
     if ((rc = check_mx(w_gate)) || (rc = check_mx(w_up)) || (rc = check_mx(w_down))) return rc;
     if (!aligned(w_gate.s, 16) || !aligned(w_up.s, 16) || !aligned(w_down.s, 16)) return MOE_ERR_ALIGN;
+    if (ns == 3) {
+        if ((rc = check_mx(*shared_gate)) || (rc = check_mx(*shared_up)) || (rc = check_mx(*shared_down))) return rc;
+        if (!aligned(shared_gate->s, 16) || !aligned(shared_up->s, 16) || !aligned(shared_down->s, 16))
+            return MOE_ERR_ALIGN;
+    }
     if (!aligned(x, 32) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(y, 8)) return MOE_ERR_ALIGN;
-    const size_t need = grouped_carve(T, k, E, d, I, nullptr, nullptr);
+    const size_t need = grouped_carve(T, k, E, d, I, ns == 3, nullptr, nullptr);
     if (!workspace || workspace_bytes < need) return MOE_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return MOE_ERR_ALIGN;
     DeviceInfo di;
@@ -354,10 +374,11 @@ int moe_layer_grouped(const void* x, int T, int d, const int32_t* topk_ids, cons
     if (align_smem_bytes(E) > (size_t)di.max_smem_optin || grouped_smem_bytes(d, I) > (size_t)di.max_smem_optin)
         return MOE_ERR_LIMIT;
     GroupedWorkspace ws{};
-    grouped_carve(T, k, E, d, I, static_cast<char*>(workspace), &ws);
+    grouped_carve(T, k, E, d, I, ns == 3, static_cast<char*>(workspace), &ws);
     return cuda_status(launch_grouped(static_cast<const uint16_t*>(x), T, d, topk_ids, topk_w, k, view(&w_gate),
-                                      view(&w_up), view(&w_down), E, I, act_mx != 0, ws,
-                                      static_cast<uint16_t*>(y), (cudaStream_t)stream));
+                                      view(&w_up), view(&w_down), view(shared_gate), view(shared_up),
+                                      view(shared_down), E, I, act_mx != 0, ws, static_cast<uint16_t*>(y),
+                                      (cudaStream_t)stream));
 }
 
 int moe_router_topk(const float* logits, int B, int E, int k, int score, float scale, int32_t* topk_ids,

@@ -455,12 +455,13 @@ __global__ void __launch_bounds__(GR_THREADS, NB == 1 ? 2 : 1) grouped_mma_kerne
     if (tid == 0 && *abort) atomicOr(a.err, MOE_DEVERR_TIMEOUT);
 }
 
-// y[t][o] = bf16( sum_j w[t][j] * out[t*k + j][o] ), j in order; a slot
-// whose expert id is outside [0, E) (never placed by the sort) adds nothing.
-// Four consecutive outputs per thread (d % 4 == 0).
+// y[t][o] = bf16( sum_j w[t][j] * out[t*k + j][o] + sh[t][o] ), j in order,
+// then the shared expert's row (weight 1; sh null without one); a slot whose
+// expert id is outside [0, E) (never placed by the sort) adds nothing.  Four
+// consecutive outputs per thread (d % 4 == 0).
 __global__ void grouped_combine_kernel(const float* __restrict__ out, const float* __restrict__ w,
-                                       const int32_t* __restrict__ ids, int T, int k, int E, int d,
-                                       uint16_t* __restrict__ y) {
+                                       const int32_t* __restrict__ ids, const float* __restrict__ sh, int T, int k,
+                                       int E, int d, uint16_t* __restrict__ y) {
     const int64_t n4 = (int64_t)T * d / 4;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t t = i * 4 / d, o = i * 4 - t * d;
@@ -474,11 +475,29 @@ __global__ void grouped_combine_kernel(const float* __restrict__ out, const floa
             acc.z = fmaf(wt, v.z, acc.z);
             acc.w = fmaf(wt, v.w, acc.w);
         }
+        if (sh) {
+            const float4 v = *reinterpret_cast<const float4*>(sh + t * d + o);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
         const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
         uint2 pk;
         memcpy(&pk.x, &lo, 4);
         memcpy(&pk.y, &hi, 4);
         *reinterpret_cast<uint2*>(y + i * 4) = pk;
+    }
+}
+
+// The shared expert's sort: every token in order, padded to whole blocks of
+// GR_BM rows, all of expert 0 (of the one-expert shared arrays).
+__global__ void grouped_shared_sort_kernel(int32_t* __restrict__ sorted, int32_t* __restrict__ expert, int32_t* ntpp,
+                                           int T, int64_t n_sh) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_sh; i += (int64_t)gridDim.x * blockDim.x) {
+        sorted[i] = i < T ? (int32_t)i : T;
+        if (i % GR_BM == 0) expert[i / GR_BM] = 0;
+        if (i == 0) *ntpp = (int32_t)n_sh;
     }
 }
 
@@ -532,19 +551,27 @@ size_t grouped_smem_bytes(int d, int I) {
 }
 
 cudaError_t launch_grouped(const uint16_t* x, int T, int d, const int32_t* ids, const float* w, int k, MXView wg,
-                           MXView wu, MXView wd, int E, int I, bool act_mx, const GroupedWorkspace& ws, uint16_t* y,
-                           cudaStream_t st) {
+                           MXView wu, MXView wd, MXView shg, MXView shu, MXView shd, int E, int I, bool act_mx,
+                           const GroupedWorkspace& ws, uint16_t* y, cudaStream_t st) {
     DeviceInfo di;
     cudaError_t err = device_info(&di);
     if (err != cudaSuccess) return err;
     int dev = 0;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-    GRMaps m1{}, m2{};
+    const bool shared = shg.w != nullptr;
+    GRMaps m1{}, m2{}, s1{}, s2{};
     if (!map_2d_u8(&m1.w0, wg.w, (uint64_t)E * I, d, GR_BN, GR_RC, true) ||
         !map_2d_u8(&m1.w1, wu.w, (uint64_t)E * I, d, GR_BN, GR_RC, true) ||
         !map_2d_u8(&m2.w0, wd.w, (uint64_t)E * d, I, GR_BN, GR_RC, true))
         return cudaErrorInvalidValue;
     m2.w1 = m2.w0;
+    if (shared) {
+        if (!map_2d_u8(&s1.w0, shg.w, (uint64_t)I, d, GR_BN, GR_RC, true) ||
+            !map_2d_u8(&s1.w1, shu.w, (uint64_t)I, d, GR_BN, GR_RC, true) ||
+            !map_2d_u8(&s2.w0, shd.w, (uint64_t)d, I, GR_BN, GR_RC, true))
+            return cudaErrorInvalidValue;
+        s2.w1 = s2.w0;
+    }
     err = launch_align(ids, T, k, E, GR_BM, ws.sorted, ws.n_sorted, ws.expert_ids, ws.n_blocks, ws.ntpp, ws.align_ws,
                        st);
     if (err != cudaSuccess) return err;
@@ -553,33 +580,45 @@ cudaError_t launch_grouped(const uint16_t* x, int T, int d, const int32_t* ids, 
         if ((err = launch_mx_requant(x, ws.x_mx, T, d, st)) != cudaSuccess) return err;
         xa = ws.x_mx;
     }
-    GRArgs a{};
-    a.sorted = ws.sorted;
-    a.expert_ids = ws.expert_ids;
-    a.ntpp = ws.ntpp;
-    a.h_sorted = ws.h_sorted;
-    a.out = ws.out;
-    a.T = T;
-    a.k = k;
-    a.E = E;
-    a.d = d;
-    a.I = I;
-    a.err = di.err_word;
-    a.a_src = xa;
-    a.s0 = wg.s;
-    a.s1 = wu.s;
-    if ((err = launch_grouped_mma<2>(a, m1, ws.n_blocks, di, dev, st)) != cudaSuccess)
-        return err;
-    // only the real rows of h_sorted were written: round those (and harmless pad-row bits) through MXFP8
-    if (act_mx && (err = launch_mx_requant(ws.h_sorted, ws.h_sorted, ws.n_sorted, I, st)) != cudaSuccess) return err;
-    a.a_src = ws.h_sorted;
-    a.s0 = wd.s;
-    a.s1 = nullptr;
-    if ((err = launch_grouped_mma<1>(a, m2, ws.n_blocks, di, dev, st)) != cudaSuccess)
-        return err;
+    // the routed experts, then (as a one-expert layer over every token) the shared one
+    for (int pass = 0; pass < (shared ? 2 : 1); ++pass) {
+        GRArgs a{};
+        const bool sp = pass == 1;
+        if (sp) {
+            const int64_t g = std::min<int64_t>((ws.n_sh + 255) / 256, (int64_t)di.sm_count * 4);
+            grouped_shared_sort_kernel<<<(unsigned)g, 256, 0, st>>>(ws.sh_sorted, ws.sh_expert, ws.sh_ntpp, T,
+                                                                   ws.n_sh);
+            if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        }
+        a.sorted = sp ? ws.sh_sorted : ws.sorted;
+        a.expert_ids = sp ? ws.sh_expert : ws.expert_ids;
+        a.ntpp = sp ? ws.sh_ntpp : ws.ntpp;
+        a.h_sorted = sp ? ws.sh_h : ws.h_sorted;
+        a.out = sp ? ws.sh_out : ws.out;
+        a.T = T;
+        a.k = sp ? 1 : k;
+        a.E = sp ? 1 : E;
+        a.d = d;
+        a.I = I;
+        a.err = di.err_word;
+        a.a_src = xa;
+        a.s0 = sp ? shg.s : wg.s;
+        a.s1 = sp ? shu.s : wu.s;
+        const int64_t nb = sp ? ws.n_sh / GR_BM : ws.n_blocks;
+        const int64_t nrows = sp ? ws.n_sh : ws.n_sorted;
+        if ((err = launch_grouped_mma<2>(a, sp ? s1 : m1, nb, di, dev, st)) != cudaSuccess) return err;
+        // only the real rows of h were written: round those (and harmless pad-row bits) through MXFP8
+        if (act_mx && (err = launch_mx_requant(a.h_sorted, a.h_sorted, nrows, I, st)) != cudaSuccess) return err;
+        a.a_src = a.h_sorted;
+        a.s0 = sp ? shd.s : wd.s;
+        a.s1 = nullptr;
+        if ((err = launch_grouped_mma<1>(a, sp ? s2 : m2, nb, di, dev, st)) != cudaSuccess) return err;
+    }
     const int64_t n = (int64_t)T * d / 4;
     const int64_t grid = std::min<int64_t>((n + 255) / 256, (int64_t)di.sm_count * 8);
-    grouped_combine_kernel<<<(unsigned)std::max<int64_t>(grid, 1), 256, 0, st>>>(ws.out, w, ids, T, k, E, d, y);
+    grouped_combine_kernel<<<(unsigned)std::max<int64_t>(grid, 1), 256, 0, st>>>(ws.out, w, ids,
+                                                                                 shared ? ws.sh_out : nullptr, T, k,
+                                                                                 E, d, y);
     return cudaGetLastError();
 }
 

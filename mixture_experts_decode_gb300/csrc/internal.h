@@ -74,12 +74,20 @@ struct GroupedWorkspace {
     uint16_t* x_mx;       // [T][d] x rounded through MXFP8 (act_mx only)
     uint16_t* h_sorted;   // [n_sorted][I] BF16
     float* out;           // [T*k][d] FP32 per-slot partial outputs
+    // the shared expert's pass (null without one): every token, in order
+    int32_t* sh_sorted;   // [n_sh] token of each row (T = pad)
+    int32_t* sh_expert;   // [n_sh / 128] all 0
+    int32_t* sh_ntpp;     // n_sh
+    int64_t n_sh;         // T rounded up to a multiple of 128
+    uint16_t* sh_h;       // [n_sh][I] BF16
+    float* sh_out;        // [T][d] FP32
 };
 constexpr int GROUPED_BLOCK = 128;  // sorted rows per block (the MMA's M)
 bool grouped_shape_ok(int d, int I);
 size_t grouped_smem_bytes(int d, int I);
+// shg / shu / shd: the shared expert's matrices ([1][rows][K]) or all null.
 cudaError_t launch_grouped(const uint16_t* x, int T, int d, const int32_t* ids, const float* w, int k, MXView wg,
-                           MXView wu, MXView wd, int E, int I, bool act_mx, const GroupedWorkspace& ws, uint16_t* y,
-                           cudaStream_t st);
+                           MXView wu, MXView wd, MXView shg, MXView shu, MXView shd, int E, int I, bool act_mx,
+                           const GroupedWorkspace& ws, uint16_t* y, cudaStream_t st);
 
 }  // namespace moedec

@@ -102,13 +102,14 @@ def _silu(g):
     return g / (1.0 + np.exp(-g))
 
 
-def h_interval(ref, abs_g, abs_u):
-    """Bounds (lo, hi) of the exact h that an FP32 evaluation may have seen."""
+def h_interval(ref, abs_g, abs_u, eps_ulps=EPS_ULPS):
+    """Bounds (lo, hi) of the exact h that an FP32 evaluation may have seen
+    (dot products within eps_ulps units of 2^-24 of sum |x * w|)."""
     g, u, h = ref["g64"], ref["u64"], ref["h64"]
     sig = 1.0 / (1.0 + np.exp(-g))
     dsilu = sig * (1.0 + g * (1.0 - sig))
-    eg = EPS_ULPS * 2.0 ** -24 * abs_g
-    eu = EPS_ULPS * 2.0 ** -24 * abs_u
+    eg = eps_ulps * 2.0 ** -24 * abs_g
+    eu = eps_ulps * 2.0 ** -24 * abs_u
     dh = np.abs(dsilu * u) * eg + np.abs(_silu(g)) * eu + eg * eu + 8 * 2.0 ** -24 * np.abs(h)
     return h - dh, h + dh
 
@@ -157,6 +158,34 @@ def abs_sums(W, x_tok, ids_tok, KS):
         for i, (b, j) in enumerate(slots):
             sg[b, j], su[b, j] = g[i], u[i]
     return sg, su
+
+
+def tc_y_allowance(W, ids_tok, w_tok, ref, x_tok, d, K_gu, K_dn):
+    """Allowance for a layer whose dot products are summed by the tensor
+    cores in FP32 (K / 16 MMA steps, each adding a 16-product partial): the
+    standard bound of recursive FP32 summation, (steps + 16) units of 2^-24
+    of the sum of the terms' magnitudes, per dot product.  Gate/up: every h
+    whose interval under that bound holds two BF16 roundings moves y by
+    sum_j |w_j| sum_i |Wd| * (round(hi) - round(lo)); down: each slot's row
+    may be off by (K_dn / 16 + 16) units of sum_i |h Wd|, times |w_j|, and
+    the combine's k + 1 additions a few units more.  Computed from the
+    oracle's values and the weights only."""
+    KS = ref["h"].shape[1]
+    k = ids_tok.shape[1]
+    ag, au = abs_sums(W, x_tok, ids_tok, KS)
+    lo, hi = h_interval(ref, ag, au, eps_ulps=K_gu / 16 + 16)
+    gap = _bf16_value(_bf16_round_vec(hi)) - _bf16_value(_bf16_round_vec(lo))
+    allow = y_allowance(W, ids_tok, w_tok, gap, d) if np.any(gap) else np.zeros((ids_tok.shape[0], d))
+    # the down products and the combine
+    habs = np.abs(_bf16_value(ref["h"]))
+    T = ids_tok.shape[0]
+    acc = np.zeros((T, d))
+    for e, slots in _slots_by_expert(ids_tok, KS).items():
+        A = abs_matrix(W, "down", e)
+        for b, j in slots:
+            wt = abs(float(w_tok[b, j])) if j < k else 1.0
+            acc[b] += wt * (A @ torch.from_numpy(habs[b, j]).to(torch.float32)).double().numpy()
+    return allow + (K_dn / 16 + 16 + k + 1) * 2.0 ** -24 * acc, int(np.count_nonzero(gap))
 
 
 def y_allowance(W, ids_tok, w_tok, gap, d):

@@ -141,18 +141,24 @@ def test_fp4_passes_reject_bad_arguments_before_launch(lib):
 def test_grouped_layer_rejects_bad_arguments_before_launch(lib):
     m = _mx()
     ws = ctypes.c_size_t()
-    assert lib.moe_layer_grouped_workspace_bytes(256, 8, 128, 2048, 768, ctypes.byref(ws)) == 0
+    assert lib.moe_layer_grouped_workspace_bytes(256, 8, 128, 2048, 768, 0, ctypes.byref(ws)) == 0
+    plain = ws.value
     ns = 256 * 8 + 128 * 127
     # at least the sort output, h for every sorted row and the FP32 per-slot outputs
     assert ws.value >= ns * 4 + ns * 768 * 2 + 256 * 8 * 2048 * 4
-    assert lib.moe_layer_grouped_workspace_bytes(4, 2, 8, 96, 256, ctypes.byref(ws)) == -2   # d % 128
-    assert lib.moe_layer_grouped_workspace_bytes(4, 2, 8, 256, 160, ctypes.byref(ws)) == -2  # I % 128
-    assert lib.moe_layer_grouped_workspace_bytes(4, 9, 8, 256, 256, ctypes.byref(ws)) == -2   # k > E
-    assert lib.moe_layer_grouped_workspace_bytes(4, 2, 1025, 256, 256, ctypes.byref(ws)) == -3
-    assert lib.moe_layer_grouped_workspace_bytes(-1, 2, 8, 256, 256, ctypes.byref(ws)) == -1
+    assert lib.moe_layer_grouped_workspace_bytes(4, 2, 8, 96, 256, 0, ctypes.byref(ws)) == -2   # d % 128
+    assert lib.moe_layer_grouped_workspace_bytes(4, 2, 8, 256, 160, 0, ctypes.byref(ws)) == -2  # I % 128
+    assert lib.moe_layer_grouped_workspace_bytes(4, 9, 8, 256, 256, 0, ctypes.byref(ws)) == -2   # k > E
+    assert lib.moe_layer_grouped_workspace_bytes(4, 2, 1025, 256, 256, 0, ctypes.byref(ws)) == -3
+    assert lib.moe_layer_grouped_workspace_bytes(-1, 2, 8, 256, 256, 0, ctypes.byref(ws)) == -1
 
-    def call(T=4, x=0x20000, ids=0x30000, w=0x40000, act=0, wsp=0x70000, wsb=1 << 40, y=0x60000):
-        return lib.moe_layer_grouped(x, T, 256, ids, w, 2, m, m, m, 8, 256, act, wsp, wsb, y, None)
+    assert lib.moe_layer_grouped_workspace_bytes(256, 8, 128, 2048, 768, 1, ctypes.byref(ws)) == 0
+    # a shared expert adds its own sort, h rows (T rounded to 128) and FP32 rows
+    assert ws.value >= plain + 256 * 768 * 2 + 256 * 2048 * 4
+
+    def call(T=4, x=0x20000, ids=0x30000, w=0x40000, act=0, wsp=0x70000, wsb=1 << 40, y=0x60000,
+             sg=None, su=None, sd=None):
+        return lib.moe_layer_grouped(x, T, 256, ids, w, 2, m, m, m, 8, 256, sg, su, sd, act, wsp, wsb, y, None)
 
     assert call(act=2) == -1
     assert call(x=0) == -1
@@ -160,3 +166,4 @@ def test_grouped_layer_rejects_bad_arguments_before_launch(lib):
     assert call(wsb=16) == -4
     assert call(wsp=0x70010) == -5                        # workspace not 256-byte aligned
     assert call(T=0, x=0) == 0                            # empty batch: no launch
+    assert call(sg=ctypes.byref(m)) == -1                 # shared expert: all three or none
