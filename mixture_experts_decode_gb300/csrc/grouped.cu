@@ -7,26 +7,29 @@
 // expert-centric packing; the align page's MoE Align & Sort feeds exactly
 // such grouped GEMMs).
 //
-//   gemm1 (gate/up): one CTA per (block of GR_BM sorted slots, GR_BN rows of
-//     I).  A = the block's real slots' token rows of x (BF16), B = the
-//     block's expert's W_gate and W_up rows, dequantised from MXFP8 to BF16
-//     in shared memory (exact for scale bytes >= 3: an E4M3 value times a
-//     power of two has at most four significant bits and stays a BF16
-//     normal), D = two FP32 accumulators in tensor memory.  Epilogue:
+//   gemm1 (gate/up): per tile (block of GR_BM sorted slots, GR_BN rows of
+//     I), the block's expert's W_gate and W_up rows, dequantised from MXFP8
+//     to BF16 in shared memory (exact for scale bytes >= 3: an E4M3 value
+//     times a power of two has at most four significant bits and stays a
+//     BF16 normal), times the block's real slots' token rows of x (BF16),
+//     into two FP32 accumulators in tensor memory.  Epilogue:
 //     h = bf16(SiLU(g) * u) per real slot, into h_sorted.
-//   gemm2 (down): A = the real slots' rows of h_sorted, B = the expert's
-//     W_down rows, D = FP32 in tensor memory; the epilogue stores each real
-//     slot's row of partial outputs (FP32) at its flat slot index.
-//   combine: y[t][o] = bf16( sum_j w[t][j] * out[t*k + j][o] ), the k slots
-//     in order.
-// Each MMA is tcgen05.mma kind::f16 (BF16 x BF16 -> FP32), M = 128, N =
-// 128, K = 16, issued by one thread from K-major 128-byte-swizzled shared
-// memory tiles; tcgen05.commit signals completion to an mbarrier.  The pad
-// rows of a block's A tile are never written: they only feed accumulator
-// rows that no epilogue stores.  The products are those of the MX values
-// exactly; sums are FP32 in the tensor core's order.  With act_mx set, x
-// and h are first rounded through MXFP8 (moe_mx_requant): the conventional
-// path's activations.
+//   gemm2 (down): the expert's W_down rows times the real slots' rows of
+//     h_sorted, FP32 in tensor memory; the epilogue stores each real slot's
+//     row of partial outputs (FP32) at its flat slot index.
+//   shared expert (when given): the same two passes as a one-expert layer
+//     over every token in order.
+//   combine: y[t][o] = bf16( sum_j w[t][j] * out[t*k + j][o] + shared[t][o] ),
+//     the k slots in order, the shared row last.
+// Each MMA is tcgen05.mma kind::f16 (BF16 x BF16 -> FP32) with the weight
+// tile as its M = 128 operand and the block's slot rows as N (the real rows
+// rounded up to 16), K = 16, issued by one thread from K-major 128-byte-
+// swizzled shared memory tiles; tcgen05.commit signals completion to an
+// mbarrier.  The pad rows of a block's slot tile are never written: they
+// only feed accumulator columns that no epilogue reads.  The products are
+// those of the MX values exactly; sums are FP32 in the tensor core's order.
+// With act_mx set, x and h are first rounded through MXFP8
+// (moe_mx_requant): the conventional path's activations.
 #include <cstdint>
 #include <mutex>
 
@@ -36,8 +39,8 @@
 
 namespace moedec {
 
-constexpr int GR_BM = GROUPED_BLOCK;       // sorted slots per block (the MMA's M)
-constexpr int GR_BN = 128;                 // weight rows per tile (the MMA's N)
+constexpr int GR_BM = GROUPED_BLOCK;       // sorted slots per block (at most the MMA's N)
+constexpr int GR_BN = 128;                 // weight rows per tile (the MMA's M)
 constexpr int GR_KC = 64;                  // K elements per chunk (one 128-byte swizzle row of BF16)
 constexpr int GR_RC = 128;                 // K elements per raw-code stage (two chunks: 128 B per row)
 constexpr int GR_RAW = GR_BN * GR_RC;      // raw-code bytes per matrix and stage

@@ -82,7 +82,7 @@ struct GroupedWorkspace {
     uint16_t* sh_h;       // [n_sh][I] BF16
     float* sh_out;        // [T][d] FP32
 };
-constexpr int GROUPED_BLOCK = 128;  // sorted rows per block (the MMA's M)
+constexpr int GROUPED_BLOCK = 128;  // sorted rows per block
 bool grouped_shape_ok(int d, int I);
 size_t grouped_smem_bytes(int d, int I);
 // shg / shu / shd: the shared expert's matrices ([1][rows][K]) or all null.
