@@ -428,10 +428,33 @@ def measure_layer(wl, stream, ranks, K, W, hbm_peak, copy_gbs, kernels=True):
     return out
 
 
+def measure_grouped(wl, stream, ranks, K):
+    """µs per moe_layer_grouped call on a workload's batches and weights
+    (shared expert included); None if the call is refused."""
+    import torch
+    import mixture_experts_decode_gb300 as moe
+    cfg = wl.cfg
+    try:
+        ws = torch.empty(moe.layer_grouped_workspace_bytes(wl.B, cfg.k, cfg.E, cfg.d, cfg.I, cfg.shared),
+                         dtype=torch.uint8, device=wl.dev)
+
+        def step(i):
+            g, u, d, sh = wl.replicas[i % wl.R]
+            j = i % len(wl.batches)
+            moe.layer_grouped(wl.x[j], wl.ids[j], wl.w[j], g, u, d, shared=sh, workspace=ws, y=wl.y)
+
+        secs, _, _ = time_steps(step, K, 3, stream, ranks, chunk=K, min_seconds=0.05, min_repeats=3, max_repeats=10)
+        del ws
+        return secs / K * 1e6
+    except Exception:  # reported as missing, never fatal to the bench line
+        return None
+
+
 def sweep(dev, stream, ranks, hbm_peak, copy_gbs, qwen_replicas):
     """Every decode config of the workload list: the Qwen3-style B sweep, the
     routing-locality sweep at B=32 (with the contiguous - scattered gap) and
-    the DeepSeek-V3-style B sweep with its shared expert."""
+    the DeepSeek-V3-style B sweep with its shared expert (at B = 32 and 64
+    also the expert-centric layer, `grouped_us`)."""
     import torch
     from mixture_experts_decode_gb300 import inputs
     out = {"qwen3": [], "locality_b32": {}, "deepseek_v3": []}
@@ -456,7 +479,10 @@ def sweep(dev, stream, ranks, hbm_peak, copy_gbs, qwen_replicas):
     for B in (1, 8, 32, 64):
         wl = Workload(inputs.DEEPSEEK_V3, B, "sigmoid_scaled", dev, n_batches=8, replicas=ds)
         ds = wl.replicas if len(wl.replicas) > len(ds) else ds
-        out["deepseek_v3"].append(measure_layer(wl, stream, ranks, 40, 5, hbm_peak, copy_gbs))
+        row = measure_layer(wl, stream, ranks, 40, 5, hbm_peak, copy_gbs)
+        if B >= 32:  # the expert-centric layer (with its shared-expert pass) on the same batches
+            row["grouped_us"] = measure_grouped(wl, stream, ranks, 20)
+        out["deepseek_v3"].append(row)
         del wl
     del ds
     torch.cuda.empty_cache()
