@@ -199,7 +199,8 @@ int moe_layer_host(const void* x_host, int B, int d, const int32_t* topk_ids_hos
  *   2. if act_mx, x is rounded through MXFP8 (moe_mx_requant) first;
  *   3. per block of 128 sorted slots and expert e:
  *        g, u = the slots' x rows times deq(Wg[e]), deq(Wu[e]) (tensor
- *        cores, BF16 operands -- exact for MXFP8 values -- FP32 sums),
+ *        cores, BF16 operands -- exact for MXFP8 values with scale bytes
+ *        >= 3 -- FP32 sums),
  *        h = bf16_rn( g * sigmoid(g) * u )  per slot;
  *   4. if act_mx, h is rounded through MXFP8;
  *   5. out[slot] = h[slot] times deq(Wd[e]) (FP32);
@@ -220,7 +221,8 @@ int moe_layer_host(const void* x_host, int B, int d, const int32_t* topk_ids_hos
  *             E*127 < 2^31.  No limit on T beyond that.
  *   act_mx    0: activations as given (the decode layer's numerics);
  *             1: x and h rounded through MXFP8, the conventional path.
- *   workspace >= moe_layer_grouped_workspace_bytes(), 256-byte aligned.
+ *   workspace >= moe_layer_grouped_workspace_bytes(..., has_shared, ...),
+ *             256-byte aligned; its layout is internal.
  *   y         BF16 [T][d], 8-byte aligned.
  * Errors: MOE_ERR_SHAPE (d or I not a multiple of 128, k > E),
  * MOE_ERR_LIMIT, MOE_ERR_WORKSPACE, MOE_ERR_ALIGN, MOE_ERR_CUDA.
