@@ -93,7 +93,7 @@ def test_grouped_shared_expert_every_token(cuda_device, T, act_mx):
 
 def test_grouped_deepseek_sampled_tokens(cuda_device):
     """DeepSeek-V3 shapes (E=256 + shared, d=7168, I=2048) at B=64: the first
-    16 tokens of a cover of every expert block (98 of the 224 distinct
+    16 tokens of a cover of every expert block (98 of the 225 distinct
     experts and the shared expert's first block); the host-side bound of the
     check costs seconds per token at these sizes."""
     W = inputs.layer_weights(inputs.DEEPSEEK_V3, cuda_device)
